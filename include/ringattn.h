@@ -1,0 +1,190 @@
+/*
+ * ringattn.h — C ABI of libringattn.so: the single-GPU hot path of Ring Attention
+ * (online-softmax merge over P virtual KV shards) for NVIDIA GB300 (sm_103a).
+ *
+ * The method. Queries of virtual device u stay put; at ring step s = 0..P-1 the
+ * device scores them against the circulating key/value shard b = (u - s) mod P,
+ *     S = Q_u K_b^T / sqrt(d_h),
+ * and folds S into a running accumulator (m, z, y) — running row max, running
+ * denominator, running unnormalised output — with the exact rescale
+ * alpha = exp(m_old - m_new); after all P shards O = y / z.
+ *   Source: "Ring Attention" (aarnphm.xyz, thoughts/ring-attention), the ring
+ *   recurrence display; the same update as "Building block: the online-softmax
+ *   trick" in "Ring Attention: Distributed Attention Across Devices"
+ *   (aicomputerinstitute chapter) and §4.4 "Online Softmax Across KV Blocks" of
+ *   "Part 4: Ring Attention" (Fofadiya).
+ * On one GPU the P devices are virtual: a shard is an index range of tensors
+ * that all sit in this GPU's memory, and "receiving" a shard is loading its tiles.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Tensors are in ORIGINAL token order whatever the shard layout (the layout is
+ *  an index map, not a permutation of memory):
+ *    q, o        [B, N, H, d]  bf16, row-major (d fastest)
+ *    k, v        [B, N, G, d]  bf16
+ *    lse, m, z   [B, H, N]     fp32
+ *    y           [B, N, H, d]  fp32
+ *  B = batch, N = seqlen, H = heads, G = kv_heads (H % G == 0; query head h
+ *  reads kv head floor(h*G/H)), d = head_dim in {64, 128}.
+ *  LSE = m + ln z (natural log of the scaled scores); a row that admitted no
+ *  key has O = 0 and LSE = -inf.
+ *  Causal masking is on global positions: query token t sees key tokens <= t
+ *  ("Ring Attention: what the near-infinite context paper actually says",
+ *  "The causal masking complication").
+ *
+ *  Pointers named q,k,v,o,lse,m,z,y,o_parts,lse_parts are DEVICE pointers,
+ *  allocated and owned by the caller, 16-byte aligned. The library allocates
+ *  no device memory; it keeps one status word in static device memory per GPU.
+ *  `stream` is a cudaStream_t (NULL = legacy default stream); every call that
+ *  takes one is asynchronous on it. Calls on one stream are ordered; the
+ *  library holds no per-call host state, so concurrent calls on different
+ *  streams are safe when their output buffers do not overlap.
+ *
+ *  Errors: argument errors are returned synchronously before any launch and
+ *  nothing is written. RA_ERR_CUDA means a CUDA call (launch or tensor-map
+ *  encode) failed. A device-side wait that exceeds its time limit makes the
+ *  kernel stop early and record RA_ERR_TIMEOUT in the status word, read with
+ *  ring_attn_last_error() after synchronising the stream. Nothing throws.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, N % P != 0, H % G != 0, misaligned */
+  RA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, or no sm_103a device */
+  RA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  RA_ERR_TIMEOUT = 4        /* a device-side wait ran out (read via ring_attn_last_error) */
+} ra_status;
+
+/* Shard layouts ("Part 4: Ring Attention" §4.3.1 for contiguous; "Ring Attention"
+ * (aarnphm.xyz): striped ownership alternates, token t -> shard t mod P). */
+typedef enum {
+  RA_LAYOUT_CONTIGUOUS = 0, /* shard u = tokens [u*S, (u+1)*S), local i -> token u*S + i */
+  RA_LAYOUT_STRIPED = 1     /* token t -> shard t mod P, local index t div P */
+} ra_layout;
+
+/* Tile classes of a (query tile, key tile) pair ("Part 4" §4.8.1 "Skipping
+ * Fully-Masked Blocks"). */
+typedef enum { RA_TILE_EMPTY = 0, RA_TILE_PARTIAL = 1, RA_TILE_FULL = 2 } ra_tile_class;
+
+/* Tile edge (rows and keys) used by the tensor-core kernels and by
+ * ring_attn_tile_classes. */
+#define RA_TILE 128
+
+typedef struct {
+  int32_t batch;      /* B >= 1 */
+  int32_t seqlen;     /* N >= 1, N % P == 0, N < 2^30 */
+  int32_t heads;      /* H >= 1 */
+  int32_t kv_heads;   /* G >= 1, H % G == 0 */
+  int32_t head_dim;   /* d in {64, 128} */
+  int32_t P;          /* number of virtual shards, 1 <= P <= N */
+  int32_t causal;     /* 0 or 1 */
+  int32_t layout;     /* ra_layout */
+  float scale;        /* score scale; 0 means 1/sqrt(d) */
+} ra_problem;
+
+/* Full ring forward: every virtual device u folds all P shards in ring order
+ * b = (u - s) mod P, s = 0..P-1, and writes O = y / z (bf16, round to nearest
+ * even) and LSE = m + ln z (fp32). Tiles that the causal mask leaves empty are
+ * skipped. Source: "Ring Attention" (aarnphm.xyz), recurrence display and
+ * O = y/z; "Part 4: Ring Attention" §4.3 and §4.8.1.
+ * q, k, v in; o, lse out (device). Errors: see conventions. */
+ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const void* v,
+                        void* o, float* lse, void* stream);
+
+/* One ring step for all virtual devices at once: device u folds shard
+ * b = (u - s) mod P into the running state (m, z, y) of its own query rows.
+ * first != 0 starts from the empty state (m = -inf, z = 0, y = 0) and ignores
+ * the input contents of m, z, y. State layout: m, z [B, H, N] fp32 with m the
+ * running max of the scaled scores (natural units, -inf when nothing was
+ * seen), y [B, N, H, d] fp32 unnormalised; rows that shard b leaves fully
+ * masked are left unchanged. Calling s over any permutation of 0..P-1 gives
+ * the same final state up to rounding ("Ring Attention: Distributed Attention
+ * Across Devices", "Building block: the online-softmax trick": any order).
+ * Source: "Ring Attention" (aarnphm.xyz), recurrence display (one step).
+ * 0 <= s < P. m, z, y are read (unless first) and written (device). */
+ra_status ring_attn_step(const ra_problem* p, int32_t s, int32_t first,
+                         const void* q, const void* k, const void* v,
+                         float* m, float* z, float* y, void* stream);
+
+/* Same contract as ring_attn_step, computed by a plain SIMT fp32 kernel
+ * (scores, exponentials and P·V in fp32 without tensor cores or bf16 rounding of
+ * the probabilities). A cross-check for the tensor-core kernels; slow. */
+ra_status ring_attn_step_simt(const ra_problem* p, int32_t s, int32_t first,
+                              const void* q, const void* k, const void* v,
+                              float* m, float* z, float* y, void* stream);
+
+/* Running state -> result: O = y / z (bf16), LSE = m + ln z (fp32); z = 0 gives
+ * O = 0, LSE = -inf. Source: "Ring Attention" (aarnphm.xyz), O = y/z; "Part 4"
+ * §4.4 FINAL. m, z, y in; o, lse out (device). */
+ra_status ring_attn_finalize(const ra_problem* p, const float* m, const float* z,
+                             const float* y, void* o, float* lse, void* stream);
+
+/* Merge n normalised partial results of the same query rows over disjoint key
+ * sets: LSE = M + ln sum_p exp(LSE_p - M) with M = max_p LSE_p, and
+ * O = sum_p exp(LSE_p - LSE) O_p; parts with LSE_p = -inf contribute nothing,
+ * all -inf gives O = 0, LSE = -inf. Source: Transformer Math "Ring Attention"
+ * (aicassindra), "The ring is a prefill algorithm" (P partial triples combined
+ * by one rescale-and-add reduction); "Ring Attention: what the near-infinite
+ * context paper actually says", "What the online softmax accumulation actually
+ * does across rounds".
+ * o_parts [n, B, N, H, d] fp32, lse_parts [n, B, H, N] fp32 in; o [B, N, H, d]
+ * bf16, lse [B, H, N] fp32 out (device). 1 <= n_parts <= 1024. */
+ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_t heads,
+                          int32_t head_dim, const float* o_parts, const float* lse_parts,
+                          void* o, float* lse, void* stream);
+
+/* Shard ownership on the HOST: owner[t], local[t] for t < N and
+ * token_of[u*S + i] (S = N/P) for the given layout. Pure host code; host
+ * pointers, each N int32. Source: as for ra_layout. */
+ra_status ring_attn_shard_map(int32_t layout, int32_t seqlen, int32_t P,
+                              int32_t* owner, int32_t* local, int32_t* token_of);
+
+/* The same three maps computed on the GPU by the index functions the kernels
+ * use; device pointers, each N int32. */
+ra_status ring_attn_shard_map_device(int32_t layout, int32_t seqlen, int32_t P,
+                                     int32_t* owner, int32_t* local, int32_t* token_of,
+                                     void* stream);
+
+/* Tile classes of the shard pair (u, b) as the kernels see them: classes
+ * [ceil(S/RA_TILE)][ceil(S/RA_TILE)] int8 (ra_tile_class), counting only rows
+ * and keys < S. Computed on the GPU by the kernels' own classifier. Source:
+ * "Part 4: Ring Attention" §4.8.1. classes: device pointer. */
+ra_status ring_attn_tile_classes(const ra_problem* p, int32_t u, int32_t b, int8_t* classes,
+                                 void* stream);
+
+/* Element mask of the shard pair (u, b): mask[i][j] = 1 iff local query i of
+ * shard u may attend to local key j of shard b, [S][S] uint8, computed on the
+ * GPU by the kernels' own per-row visibility rule. mask: device pointer. */
+ra_status ring_attn_mask(const ra_problem* p, int32_t u, int32_t b, uint8_t* mask,
+                         void* stream);
+
+/* Reads and clears the calling GPU's status word. *device_code receives the
+ * ra_status a kernel recorded (RA_OK if none). Synchronises with the device's
+ * legacy stream; call after synchronising the stream of interest. */
+ra_status ring_attn_last_error(int32_t* device_code);
+
+/* Launches a one-warp kernel that waits, with the library's bounded wait, on a
+ * barrier that nothing completes, for at most limit_ns nanoseconds; it then
+ * records RA_ERR_TIMEOUT in the status word and returns. Lets a test see the
+ * timeout path without a hang. 0 < limit_ns <= 10^9. */
+ra_status ring_attn_selftest_timeout(uint64_t limit_ns, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* ra_status_str(ra_status s);
+
+/* Library ABI version (major*100 + minor). */
+int32_t ring_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

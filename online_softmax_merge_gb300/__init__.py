@@ -1,0 +1,233 @@
+"""Ring Attention's online-softmax merge on one GB300: Python binding.
+
+Thin wrappers over the C ABI of libringattn.so (include/ringattn.h). They check
+shapes, dtypes and devices, allocate outputs with PyTorch when none are given,
+and pass raw pointers plus the current CUDA stream. Every step of the path runs
+in the library's CUDA kernels; nothing here computes attention.
+
+Tensor layouts (original token order, whatever the shard layout):
+  q, o [B, N, H, d] bf16;  k, v [B, N, G, d] bf16;  lse, m, z [B, H, N] fp32;
+  y [B, N, H, d] fp32;  o_parts [n, B, N, H, d] fp32;  lse_parts [n, B, H, N] fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import (LAYOUTS, RA_ERR_CUDA, RA_ERR_INVALID_ARG, RA_ERR_TIMEOUT,  # noqa: F401
+                   RA_ERR_UNSUPPORTED, RA_OK, TILE, RingAttnError, check, load)
+
+__all__ = ["fwd", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
+           "tile_classes", "mask", "last_error", "selftest_timeout", "problem", "RingAttnError",
+           "empty_state", "LAYOUTS", "TILE"]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def problem(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int, P: int,
+            causal: bool, layout: str = "contiguous", scale: float = 0.0) -> _lib.RaProblem:
+    """The ra_problem struct (scale 0 means 1/sqrt(head_dim))."""
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout must be one of {tuple(LAYOUTS)}")
+    return _lib.RaProblem(batch, seqlen, heads, kv_heads, head_dim, P, int(bool(causal)),
+                          LAYOUTS[layout], float(scale))
+
+
+def _qkv_problem(q, k, v, P, layout, causal, scale):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, N, H, d] and k, v [B, N, G, d]")
+    B, N, H, d = q.shape
+    G = k.shape[2]
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, (B, N, G, d))
+    _need(v, "v", torch.bfloat16, (B, N, G, d))
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    return problem(B, N, H, G, d, P, causal, layout, scale), (B, N, H, G, d)
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str = "contiguous",
+        causal: bool = True, scale: float = 0.0, out: Optional[torch.Tensor] = None,
+        lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Full ring forward over P virtual shards (ring_attn_fwd). Returns (O, LSE)."""
+    lib = load()
+    pr, (B, N, H, G, d) = _qkv_problem(q, k, v, P, layout, causal, scale)
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, N, H, d))
+    _need(lse, "lse", torch.float32, (B, H, N))
+    with torch.cuda.device(q.device):
+        check("ring_attn_fwd", lib.ring_attn_fwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v),
+                                                 _ptr(out), _ptr(lse), _stream(q.device)))
+    return out, lse
+
+
+def empty_state(q: torch.Tensor):
+    """Uninitialised (m, z, y) buffers for the step API (start with first=True)."""
+    B, N, H, d = q.shape
+    m = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    z = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    y = torch.empty((B, N, H, d), dtype=torch.float32, device=q.device)
+    return m, z, y
+
+
+def _step(fn_name, q, k, v, P, s, state, first, layout, causal, scale):
+    lib = load()
+    pr, (B, N, H, G, d) = _qkv_problem(q, k, v, P, layout, causal, scale)
+    m, z, y = state
+    _need(m, "m", torch.float32, (B, H, N))
+    _need(z, "z", torch.float32, (B, H, N))
+    _need(y, "y", torch.float32, (B, N, H, d))
+    with torch.cuda.device(q.device):
+        check(fn_name, getattr(lib, fn_name)(ctypes.byref(pr), int(s), int(bool(first)), _ptr(q),
+                                             _ptr(k), _ptr(v), _ptr(m), _ptr(z), _ptr(y),
+                                             _stream(q.device)))
+    return state
+
+
+def step(q, k, v, P: int, s: int, state, first: bool, layout: str = "contiguous",
+         causal: bool = True, scale: float = 0.0):
+    """One ring step s for every virtual device (ring_attn_step); updates state in place."""
+    return _step("ring_attn_step", q, k, v, P, s, state, first, layout, causal, scale)
+
+
+def step_simt(q, k, v, P: int, s: int, state, first: bool, layout: str = "contiguous",
+              causal: bool = True, scale: float = 0.0):
+    """ring_attn_step_simt: the fp32 SIMT cross-check of step()."""
+    return _step("ring_attn_step_simt", q, k, v, P, s, state, first, layout, causal, scale)
+
+
+def finalize(state, P: int = 1, layout: str = "contiguous", causal: bool = True,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """(m, z, y) -> (O, LSE) (ring_attn_finalize)."""
+    lib = load()
+    m, z, y = state
+    B, N, H, d = y.shape
+    _need(y, "y", torch.float32)
+    _need(m, "m", torch.float32, (B, H, N))
+    _need(z, "z", torch.float32, (B, H, N))
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=y.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=y.device)
+    _need(out, "out", torch.bfloat16, (B, N, H, d))
+    _need(lse, "lse", torch.float32, (B, H, N))
+    pr = problem(B, N, H, H, d, P, causal, layout)
+    with torch.cuda.device(y.device):
+        check("ring_attn_finalize", lib.ring_attn_finalize(ctypes.byref(pr), _ptr(m), _ptr(z),
+                                                           _ptr(y), _ptr(out), _ptr(lse),
+                                                           _stream(y.device)))
+    return out, lse
+
+
+def merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: Optional[torch.Tensor] = None,
+          lse: Optional[torch.Tensor] = None):
+    """Merge n normalised partials (ring_attn_merge). Returns (O bf16, LSE fp32)."""
+    lib = load()
+    if o_parts.dim() != 5:
+        raise ValueError("o_parts must be [n, B, N, H, d]")
+    n, B, N, H, d = o_parts.shape
+    _need(o_parts, "o_parts", torch.float32)
+    _need(lse_parts, "lse_parts", torch.float32, (n, B, H, N))
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device)
+    _need(out, "out", torch.bfloat16, (B, N, H, d))
+    _need(lse, "lse", torch.float32, (B, H, N))
+    with torch.cuda.device(o_parts.device):
+        check("ring_attn_merge", lib.ring_attn_merge(n, B, N, H, d, _ptr(o_parts), _ptr(lse_parts),
+                                                     _ptr(out), _ptr(lse),
+                                                     _stream(o_parts.device)))
+    return out, lse
+
+
+def shard_map(layout: str, seqlen: int, P: int):
+    """Host shard maps (ring_attn_shard_map): owner[N], local[N], token_of[N] lists."""
+    lib = load()
+    arr = ctypes.c_int32 * seqlen
+    own, loc, tok = arr(), arr(), arr()
+    check("ring_attn_shard_map", lib.ring_attn_shard_map(LAYOUTS[layout], seqlen, P, own, loc,
+                                                         tok))
+    return list(own), list(loc), list(tok)
+
+
+def shard_map_device(layout: str, seqlen: int, P: int, device="cuda"):
+    """The same maps computed on the GPU (ring_attn_shard_map_device), as int32 tensors."""
+    lib = load()
+    device = torch.device(device)
+    own = torch.empty(seqlen, dtype=torch.int32, device=device)
+    loc = torch.empty_like(own)
+    tok = torch.empty_like(own)
+    with torch.cuda.device(device):
+        check("ring_attn_shard_map_device",
+              lib.ring_attn_shard_map_device(LAYOUTS[layout], seqlen, P, _ptr(own), _ptr(loc),
+                                             _ptr(tok), _stream(device)))
+    return own, loc, tok
+
+
+def tile_classes(pr: _lib.RaProblem, u: int, b: int, device="cuda") -> torch.Tensor:
+    """Tile classes of shard pair (u, b) as the kernels see them (int8 [nt, nt])."""
+    lib = load()
+    device = torch.device(device)
+    S = pr.seqlen // pr.P
+    nt = (S + TILE - 1) // TILE
+    out = torch.empty((nt, nt), dtype=torch.int8, device=device)
+    with torch.cuda.device(device):
+        check("ring_attn_tile_classes",
+              lib.ring_attn_tile_classes(ctypes.byref(pr), u, b, _ptr(out), _stream(device)))
+    return out
+
+
+def mask(pr: _lib.RaProblem, u: int, b: int, device="cuda") -> torch.Tensor:
+    """Element mask of shard pair (u, b) from the kernels' visibility rule (uint8 [S, S])."""
+    lib = load()
+    device = torch.device(device)
+    S = pr.seqlen // pr.P
+    out = torch.empty((S, S), dtype=torch.uint8, device=device)
+    with torch.cuda.device(device):
+        check("ring_attn_mask", lib.ring_attn_mask(ctypes.byref(pr), u, b, _ptr(out),
+                                                   _stream(device)))
+    return out
+
+
+def last_error(device="cuda") -> int:
+    """Read and clear the GPU's status word (call after synchronising)."""
+    lib = load()
+    code = ctypes.c_int32(0)
+    with torch.cuda.device(torch.device(device)):
+        check("ring_attn_last_error", lib.ring_attn_last_error(ctypes.byref(code)))
+    return int(code.value)
+
+
+def selftest_timeout(limit_ns: int, device="cuda") -> None:
+    """Launch the bounded-wait self test (it records RA_ERR_TIMEOUT after limit_ns)."""
+    lib = load()
+    device = torch.device(device)
+    with torch.cuda.device(device):
+        check("ring_attn_selftest_timeout",
+              lib.ring_attn_selftest_timeout(int(limit_ns), _stream(device)))

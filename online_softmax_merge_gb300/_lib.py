@@ -1,0 +1,76 @@
+"""ctypes loader for libringattn.so (the C ABI in include/ringattn.h).
+
+Loading fails loudly when the library has not been built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libringattn.so")
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
+STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
+                4: "RA_ERR_TIMEOUT"}
+LAYOUTS = {"contiguous": 0, "striped": 1}
+TILE = 128
+
+# Every exported function of include/ringattn.h, with (restype, argtypes).
+_i32, _u64, _vp, _fp = ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p
+
+
+class RaProblem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("P", ctypes.c_int32),
+                ("causal", ctypes.c_int32), ("layout", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+_PP = ctypes.POINTER(RaProblem)
+SIGNATURES = {
+    "ring_attn_fwd": (_i32, [_PP, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_step": (_i32, [_PP, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_step_simt": (_i32, [_PP, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_finalize": (_i32, [_PP, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_merge": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_shard_map": (_i32, [_i32, _i32, _i32, _vp, _vp, _vp]),
+    "ring_attn_shard_map_device": (_i32, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "ring_attn_tile_classes": (_i32, [_PP, _i32, _i32, _vp, _vp]),
+    "ring_attn_mask": (_i32, [_PP, _i32, _i32, _vp, _vp]),
+    "ring_attn_last_error": (_i32, [ctypes.POINTER(ctypes.c_int32)]),
+    "ring_attn_selftest_timeout": (_i32, [_u64, _vp]),
+    "ra_status_str": (ctypes.c_char_p, [_i32]),
+    "ring_attn_version": (_i32, []),
+}
+
+_LIB = None
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(code, code)}")
+        self.fn = fn
+        self.code = code
+
+
+def load() -> ctypes.CDLL:
+    """Load (once) and return the library; raises if it is not built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or python online_softmax_merge_gb300/build.py) first")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def check(fn: str, code: int) -> None:
+    if code != RA_OK:
+        raise RingAttnError(fn, code)

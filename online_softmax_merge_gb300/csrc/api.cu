@@ -1,0 +1,386 @@
+// C ABI of libringattn.so (declared in include/ringattn.h): argument checks,
+// status word, TMA tensor maps, and launches. No device memory is allocated
+// here; the only device state is one static status word per GPU.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+#include "shardmap.cuh"
+
+using namespace ra;
+
+namespace {
+
+// Status word of the GPU: a kernel that gives up on a wait records its code here.
+__device__ int g_status = 0;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single device-side wait
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  bool init = false;
+  bool sm103 = false;
+  int* status = nullptr;
+};
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+// Current device's facts; RA_ERR_UNSUPPORTED unless it is compute capability 10.3.
+ra_status current_device(DevInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return RA_ERR_CUDA;
+    d.sm103 = (major == 10 && minor == 3);
+    if (d.sm103) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return RA_ERR_CUDA;
+      d.status = static_cast<int*>(ptr);
+    }
+    d.init = true;
+  }
+  *out = &d;
+  return d.sm103 ? RA_OK : RA_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ra_status check_problem(const ra_problem* pr) {
+  if (pr == nullptr) return RA_ERR_INVALID_ARG;
+  if (pr->batch < 1 || pr->seqlen < 1 || pr->heads < 1 || pr->kv_heads < 1 || pr->P < 1)
+    return RA_ERR_INVALID_ARG;
+  if (pr->seqlen >= (1 << 30) || pr->P > pr->seqlen || pr->seqlen % pr->P != 0)
+    return RA_ERR_INVALID_ARG;
+  if (pr->heads % pr->kv_heads != 0) return RA_ERR_INVALID_ARG;
+  if (pr->causal != 0 && pr->causal != 1) return RA_ERR_INVALID_ARG;
+  if (pr->layout != RA_LAYOUT_CONTIGUOUS && pr->layout != RA_LAYOUT_STRIPED)
+    return RA_ERR_INVALID_ARG;
+  if (!(pr->scale >= 0.f) || isinf(pr->scale)) return RA_ERR_INVALID_ARG;
+  if (pr->head_dim != 64 && pr->head_dim != 128) return RA_ERR_UNSUPPORTED;
+  // every tensor's element count must fit the kernels' 64-bit offsets and the
+  // tensor-map extents (< 2^32 per dimension)
+  const double elems = static_cast<double>(pr->batch) * pr->seqlen * pr->heads * pr->head_dim;
+  if (elems > 9.0e15) return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
+void fill_params(const ra_problem* pr, RingParams* p) {
+  memset(p, 0, sizeof(*p));
+  p->B = pr->batch;
+  p->N = pr->seqlen;
+  p->H = pr->heads;
+  p->G = pr->kv_heads;
+  p->D = pr->head_dim;
+  p->P = pr->P;
+  p->S = pr->seqlen / pr->P;
+  p->layout = pr->layout;
+  p->causal = pr->causal;
+  const int hpg = p->H / p->G;
+  p->pair_heads = (hpg % 2 == 0) ? 1 : 0;
+  p->nq = (p->S + 127) / 128;
+  if (p->pair_heads) {
+    p->pairs_per_g = hpg / 2;
+    p->nqq = p->nq;
+  } else {
+    p->pairs_per_g = hpg;
+    p->nqq = (p->nq + 1) / 2;
+  }
+  p->units_per_bg = p->pairs_per_g * p->P * p->nqq;
+  const double sc = pr->scale > 0.f ? static_cast<double>(pr->scale) : 1.0 / sqrt(static_cast<double>(p->D));
+  p->scale = static_cast<float>(sc);
+  p->scale_log2 = static_cast<float>(sc * 1.4426950408889634);
+  p->timeout_ns = kWaitLimitNs;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Tensor map over a [B, N, heads, D] bf16 tensor seen as 5-D (innermost first):
+// contiguous (D, heads, S, P, B) — token = u*S + i; striped (D, heads, P, S, B) —
+// token = i*P + u. A box is 64 columns of one head over 128 local rows of one
+// shard, written to shared memory with the 128-byte swizzle.
+bool encode_rows(CUtensorMap* m, const void* base, int B, int N, int heads, int D, int S, int P,
+                 int layout) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t tok = static_cast<cuuint64_t>(heads) * D * 2;
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5];
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  dims[0] = D;
+  dims[1] = heads;
+  box[0] = 64;
+  box[1] = 1;
+  strides[0] = static_cast<cuuint64_t>(D) * 2;
+  if (layout == kContiguous) {
+    dims[2] = S;
+    dims[3] = P;
+    strides[1] = tok;
+    strides[2] = tok * S;
+    box[2] = 128;
+    box[3] = 1;
+  } else {
+    dims[2] = P;
+    dims[3] = S;
+    strides[1] = tok;
+    strides[2] = tok * P;
+    box[2] = 1;
+    box[3] = 128;
+  }
+  dims[4] = B;
+  strides[3] = tok * N;
+  box[4] = 1;
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+ra_status launch_result(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
+
+ra_status run_tc(const RingParams& p, cudaStream_t st) {
+  CUtensorMap tq, tk, tv;
+  if (!encode_rows(&tq, p.q, p.B, p.N, p.H, p.D, p.S, p.P, p.layout) ||
+      !encode_rows(&tk, p.k, p.B, p.N, p.G, p.D, p.S, p.P, p.layout) ||
+      !encode_rows(&tv, p.v, p.B, p.N, p.G, p.D, p.S, p.P, p.layout))
+    return RA_ERR_CUDA;
+  return launch_result(launch_ring_tc(p, tq, tk, tv, st));
+}
+
+ra_status check_step_args(const ra_problem* pr, int32_t s, const void* q, const void* k,
+                          const void* v, float* m, float* z, float* y) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  if (s < 0 || s >= pr->P) return RA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !m || !z || !y) return RA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(m) || !aligned16(z) ||
+      !aligned16(y))
+    return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ring_attn_fwd(const ra_problem* pr, const void* q, const void* k, const void* v,
+                        void* o, float* lse, void* stream) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams p;
+  fill_params(pr, &p);
+  p.s_begin = 0;
+  p.s_end = p.P;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.status = d->status;
+  return run_tc(p, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_step(const ra_problem* pr, int32_t s, int32_t first, const void* q,
+                         const void* k, const void* v, float* m, float* z, float* y,
+                         void* stream) {
+  ra_status st = check_step_args(pr, s, q, k, v, m, z, y);
+  if (st != RA_OK) return st;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams p;
+  fill_params(pr, &p);
+  p.s_begin = s;
+  p.s_end = s + 1;
+  p.step_mode = 1;
+  p.load_state = first ? 0 : 1;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.m = m;
+  p.z = z;
+  p.y = y;
+  p.status = d->status;
+  return run_tc(p, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_step_simt(const ra_problem* pr, int32_t s, int32_t first, const void* q,
+                              const void* k, const void* v, float* m, float* z, float* y,
+                              void* stream) {
+  ra_status st = check_step_args(pr, s, q, k, v, m, z, y);
+  if (st != RA_OK) return st;
+  if (static_cast<long long>(pr->batch) * pr->heads > 65535 || pr->P > 65535)
+    return RA_ERR_UNSUPPORTED;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams p;
+  fill_params(pr, &p);
+  p.s_begin = s;
+  p.s_end = s + 1;
+  p.step_mode = 1;
+  p.load_state = first ? 0 : 1;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.m = m;
+  p.z = z;
+  p.y = y;
+  p.status = d->status;
+  return launch_result(launch_ring_simt(p, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_finalize(const ra_problem* pr, const float* m, const float* z,
+                             const float* y, void* o, float* lse, void* stream) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  if (!m || !z || !y || !o || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned16(m) || !aligned16(z) || !aligned16(y) || !aligned16(o) || !aligned16(lse))
+    return RA_ERR_INVALID_ARG;
+  if (static_cast<long long>(pr->batch) > 65535 || pr->heads > 65535) return RA_ERR_UNSUPPORTED;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams p;
+  fill_params(pr, &p);
+  p.m = const_cast<float*>(m);
+  p.z = const_cast<float*>(z);
+  p.y = const_cast<float*>(y);
+  p.o = o;
+  p.lse = lse;
+  p.status = d->status;
+  return launch_result(launch_finalize(p, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_t heads,
+                          int32_t head_dim, const float* o_parts, const float* lse_parts,
+                          void* o, float* lse, void* stream) {
+  if (n_parts < 1 || n_parts > 1024 || batch < 1 || seqlen < 1 || heads < 1)
+    return RA_ERR_INVALID_ARG;
+  if (batch > 65535 || heads > 65535) return RA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return RA_ERR_UNSUPPORTED;
+  if (!o_parts || !lse_parts || !o || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse))
+    return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  ra_status st = current_device(&d);
+  if (st != RA_OK) return st;
+  return launch_result(launch_merge(n_parts, batch, seqlen, heads, head_dim, o_parts, lse_parts,
+                                    o, lse, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_shard_map(int32_t layout, int32_t seqlen, int32_t P, int32_t* owner,
+                              int32_t* local, int32_t* token_of) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED) return RA_ERR_INVALID_ARG;
+  if (seqlen < 1 || P < 1 || P > seqlen || seqlen % P != 0 || seqlen >= (1 << 30))
+    return RA_ERR_INVALID_ARG;
+  if (!owner || !local || !token_of) return RA_ERR_INVALID_ARG;
+  const int32_t S = seqlen / P;
+  for (int32_t t = 0; t < seqlen; ++t) {
+    owner[t] = owner_of(layout, S, P, t);
+    local[t] = local_of(layout, S, P, t);
+    token_of[t] = pos_of(layout, S, P, t / S, t % S);
+  }
+  return RA_OK;
+}
+
+ra_status ring_attn_shard_map_device(int32_t layout, int32_t seqlen, int32_t P, int32_t* owner,
+                                     int32_t* local, int32_t* token_of, void* stream) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED) return RA_ERR_INVALID_ARG;
+  if (seqlen < 1 || P < 1 || P > seqlen || seqlen % P != 0 || seqlen >= (1 << 30))
+    return RA_ERR_INVALID_ARG;
+  if (!owner || !local || !token_of) return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  ra_status st = current_device(&d);
+  if (st != RA_OK) return st;
+  return launch_result(
+      launch_shard_map(layout, seqlen, P, owner, local, token_of, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_tile_classes(const ra_problem* pr, int32_t u, int32_t b, int8_t* classes,
+                                 void* stream) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  if (u < 0 || u >= pr->P || b < 0 || b >= pr->P || classes == nullptr) return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams p;
+  fill_params(pr, &p);
+  return launch_result(launch_tile_classes(p, u, b, classes, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_mask(const ra_problem* pr, int32_t u, int32_t b, uint8_t* mask,
+                         void* stream) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  if (u < 0 || u >= pr->P || b < 0 || b >= pr->P || mask == nullptr) return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams p;
+  fill_params(pr, &p);
+  return launch_result(launch_mask(p, u, b, mask, static_cast<cudaStream_t>(stream)));
+}
+
+ra_status ring_attn_last_error(int32_t* device_code) {
+  if (device_code == nullptr) return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  ra_status st = current_device(&d);
+  if (st != RA_OK) return st;
+  int code = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&code, g_status, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
+  *device_code = code;
+  return RA_OK;
+}
+
+ra_status ring_attn_selftest_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  ra_status st = current_device(&d);
+  if (st != RA_OK) return st;
+  return launch_result(launch_selftest_timeout(limit_ns, d->status, static_cast<cudaStream_t>(stream)));
+}
+
+const char* ra_status_str(ra_status s) {
+  switch (s) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID_ARG: return "RA_ERR_INVALID_ARG";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA";
+    case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+  }
+  return "RA_ERR_UNKNOWN";
+}
+
+int32_t ring_attn_version(void) { return 100; }
+
+}  // extern "C"

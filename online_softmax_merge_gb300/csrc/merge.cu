@@ -1,0 +1,206 @@
+// Bandwidth-bound kernels over per-row results: the merge of n normalised
+// partials (O_p, LSE_p) and the finalize of a running state (m, z, y).
+//
+// Merge — Transformer Math "Ring Attention" (aicassindra), "The ring is a prefill
+// algorithm": P partial (m, l, o) triples of the same rows are combined by one
+// rescale-and-add reduction. With normalised partials O_p = y_p / z_p and
+// LSE_p = m_p + ln z_p:  LSE = M + ln sum_p e^{LSE_p - M} (M = max_p LSE_p) and
+// O = sum_p e^{LSE_p - LSE} O_p. Finalize — "Ring Attention" (aarnphm.xyz):
+// O = y / z; LSE = m + ln z.
+//
+// Layout: a block owns 32 consecutive tokens of one (batch, head). Its first warp
+// reduces the 32 rows' log-sum-exps (lane = token, coalesced over tokens for each
+// part); then each warp streams whole rows: a row of d fp32 is one coalesced
+// 16-byte-per-lane (d = 128) or 8-byte-per-lane (d = 64) load per part, several
+// parts in flight per lane.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kTok = 32;      // tokens per block
+constexpr int kWarps = 8;     // 4 tokens per warp
+
+template <int D>
+struct Vec;
+template <>
+struct Vec<128> {
+  using T = float4;
+  static constexpr int kN = 4;
+};
+template <>
+struct Vec<64> {
+  using T = float2;
+  static constexpr int kN = 2;
+};
+
+__device__ __forceinline__ void load_vec(const float4* p, float (&r)[4]) {
+  const float4 v = __ldcs(p);
+  r[0] = v.x; r[1] = v.y; r[2] = v.z; r[3] = v.w;
+}
+__device__ __forceinline__ void load_vec(const float2* p, float (&r)[2]) {
+  const float2 v = __ldcs(p);
+  r[0] = v.x; r[1] = v.y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+merge_kernel(int n, int B, int N, int H, const float* __restrict__ o_parts,
+             const float* __restrict__ lse_parts, __nv_bfloat16* __restrict__ o,
+             float* __restrict__ lse) {
+  using V = Vec<D>;
+  constexpr int kN = V::kN;
+  __shared__ float s_lse[kTok];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kTok;
+  const int head = blockIdx.y;
+  const int bat = blockIdx.z;
+  const size_t part_lse = static_cast<size_t>(B) * H * N;           // stride between parts
+  const size_t part_o = static_cast<size_t>(B) * N * H * D;
+  const size_t lrow = (static_cast<size_t>(bat) * H + head) * N;    // [B,H,N] row base
+
+  if (warp == 0) {
+    const int t = t0 + lane;
+    float M = -INFINITY, acc = 0.f;
+    if (t < N) {
+      // online log-sum-exp over the parts
+      for (int q = 0; q < n; ++q) {
+        const float l = __ldcs(lse_parts + q * part_lse + lrow + t);
+        if (l == -INFINITY) continue;
+        if (l > M) {
+          acc = acc * expf(M - l) + 1.f;
+          M = l;
+        } else {
+          acc += expf(l - M);
+        }
+      }
+    }
+    const float L = (M == -INFINITY) ? -INFINITY : M + logf(acc);
+    s_lse[lane] = L;
+    if (t < N) lse[lrow + t] = L;
+  }
+  __syncthreads();
+
+  for (int tt = warp; tt < kTok; tt += kWarps) {
+    const int t = t0 + tt;
+    if (t >= N) break;
+    const float L = s_lse[tt];
+    const size_t orow = ((static_cast<size_t>(bat) * N + t) * H + head) * D;
+    float acc[kN];
+#pragma unroll
+    for (int e = 0; e < kN; ++e) acc[e] = 0.f;
+    if (L != -INFINITY) {
+      const typename V::T* src =
+          reinterpret_cast<const typename V::T*>(o_parts + orow) + lane;
+      int q = 0;
+      for (; q + 4 <= n; q += 4) {
+        float r[4][kN];
+        float wgt[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          load_vec(src + (q + k) * (part_o / kN), r[k]);
+          wgt[k] = expf(__ldg(lse_parts + (q + k) * part_lse + lrow + t) - L);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int e = 0; e < kN; ++e) acc[e] = fmaf(wgt[k], r[k][e], acc[e]);
+      }
+      for (; q < n; ++q) {
+        float r[kN];
+        load_vec(src + q * (part_o / kN), r);
+        const float wgt = expf(__ldg(lse_parts + q * part_lse + lrow + t) - L);
+#pragma unroll
+        for (int e = 0; e < kN; ++e) acc[e] = fmaf(wgt, r[e], acc[e]);
+      }
+    }
+    __nv_bfloat16* dst = o + orow + lane * kN;
+    if (kN == 4) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[kN - 2], acc[kN - 1]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&a);
+      pk.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
+      *reinterpret_cast<__nv_bfloat162*>(dst) = a;
+    }
+  }
+}
+
+// (m, z, y) -> O = y / z (bf16), LSE = m + ln z; z = 0 gives O = 0, LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32)
+finalize_kernel(int N, int H, const float* __restrict__ m, const float* __restrict__ z,
+                const float* __restrict__ y, __nv_bfloat16* __restrict__ o,
+                float* __restrict__ lse) {
+  using V = Vec<D>;
+  constexpr int kN = V::kN;
+  __shared__ float s_inv[kTok];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kTok;
+  const int head = blockIdx.y;
+  const int bat = blockIdx.z;
+  const size_t lrow = (static_cast<size_t>(bat) * H + head) * N;
+  if (warp == 0) {
+    const int t = t0 + lane;
+    float inv = 0.f;
+    if (t < N) {
+      const float zz = z[lrow + t];
+      const float mm = m[lrow + t];
+      inv = zz > 0.f ? 1.f / zz : 0.f;
+      lse[lrow + t] = zz > 0.f ? mm + logf(zz) : -INFINITY;
+    }
+    s_inv[lane] = inv;
+  }
+  __syncthreads();
+  for (int tt = warp; tt < kTok; tt += kWarps) {
+    const int t = t0 + tt;
+    if (t >= N) break;
+    const float inv = s_inv[tt];
+    const size_t orow = ((static_cast<size_t>(bat) * N + t) * H + head) * D;
+    float r[kN];
+    load_vec(reinterpret_cast<const typename V::T*>(y + orow) + lane, r);
+    __nv_bfloat16* dst = o + orow + lane * kN;
+    if (kN == 4) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(r[0] * inv, r[1] * inv);
+      __nv_bfloat162 b = __floats2bfloat162_rn(r[kN - 2] * inv, r[kN - 1] * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&a);
+      pk.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(r[0] * inv, r[1] * inv);
+      *reinterpret_cast<__nv_bfloat162*>(dst) = a;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge(int n, int B, int N, int H, int D, const float* o_parts,
+                         const float* lse_parts, void* o, float* lse, cudaStream_t st) {
+  const dim3 grid((N + kTok - 1) / kTok, H, B);
+  auto* ob = static_cast<__nv_bfloat16*>(o);
+  if (D == 64)
+    merge_kernel<64><<<grid, kWarps * 32, 0, st>>>(n, B, N, H, o_parts, lse_parts, ob, lse);
+  else
+    merge_kernel<128><<<grid, kWarps * 32, 0, st>>>(n, B, N, H, o_parts, lse_parts, ob, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const RingParams& p, cudaStream_t st) {
+  const dim3 grid((p.N + kTok - 1) / kTok, p.H, p.B);
+  auto* ob = static_cast<__nv_bfloat16*>(p.o);
+  if (p.D == 64)
+    finalize_kernel<64><<<grid, kWarps * 32, 0, st>>>(p.N, p.H, p.m, p.z, p.y, ob, p.lse);
+  else
+    finalize_kernel<128><<<grid, kWarps * 32, 0, st>>>(p.N, p.H, p.m, p.z, p.y, ob, p.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,568 @@
+// Tensor-core ring kernel for sm_103a: the fused forward (all P ring steps, then
+// O = y / z and LSE) and the single ring step over an HBM-resident (m, z, y).
+//
+// What it computes — "Ring Attention" (aarnphm.xyz), the ring recurrence display:
+// virtual device u keeps its query shard; at step s it scores the queries against
+// shard b = (u - s) mod P, S = Q_u K_b^T / sqrt(d_h), and folds S into the running
+// (m, z, y) with the rescale exp(m_old - m_new); O = y / z at the end. The same
+// update is §4.4 of "Part 4: Ring Attention" (Fofadiya). Key/value tiles that the
+// causal mask leaves empty are never loaded ("Part 4" §4.8.1).
+//
+// How, on one GB300 SM (one CTA per SM, 10 warps):
+//  * a CTA owns two 128-row query sub-tiles that read the same K/V tiles: two
+//    query heads of one GQA group at the same rows, or (when a group has an odd
+//    number of heads) two consecutive row tiles of one head;
+//  * warp 9 (TMA producer) loads both Q sub-tiles once, then streams 128-key K and
+//    V tiles of the visited shards through two shared-memory stages each, in the
+//    ring order, skipping key tiles that no query of the CTA may see;
+//  * warp 8 issues the tcgen05 MMAs from one thread: S_i = Q_i K^T into TMEM
+//    (fp32, 128 columns per sub-tile) and O_i += P_i V with P_i read from TMEM;
+//  * warps 0-3 / 4-7 are the softmax groups of sub-tile 0 / 1: one thread per
+//    query row reads its S row from TMEM, applies the causal / tail mask, updates
+//    the running max and denominator in fp32, rescales its O row in TMEM when the
+//    max grows, and writes P = exp(S - m) as bf16 back over S for the P·V MMA;
+//  * the MMA order PV_0(t), S_0(t+1), PV_1(t), S_1(t+1) lets each softmax group
+//    work while the tensor core serves the other group, and the commit that
+//    signals S_i(t+1) also proves PV_i(t) finished, so O_i is stable when read.
+// All arithmetic of the running state is fp32; exponentials use exp2 with
+// log2(e) folded into the score scale; P is rounded to bf16 for the MMA.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "shardmap.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s to let in-flight copies land on abort
+
+template <int D>
+struct Smem {
+  static constexpr int kChunk = 128 * 128;          // 128 rows x 64 bf16 (128 B, swizzled)
+  static constexpr int kTile = (D / 64) * kChunk;   // one [128 x D] bf16 tile
+  static constexpr int kQ = 0;                      // query sub-tiles 0, 1
+  static constexpr int kK = 2 * kTile;              // K stages 0, 1
+  static constexpr int kV = 4 * kTile;              // V stages 0, 1
+  static constexpr int kBar = 6 * kTile;            // mbarriers, TMEM base, abort flag
+  static constexpr int kBytes = kBar + 256;
+  // Keep one CTA per SM (it owns all 512 TMEM columns) and leave room to align.
+  static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+  static constexpr uint32_t kOcol = 256;            // TMEM: S0 [0,128) S1 [128,256) O0 O1
+};
+
+enum : int {
+  kBarQ = 0, kBarKF = 1, kBarKE = 3, kBarVF = 5, kBarVE = 7, kBarSF = 9, kBarPF = 11,
+  kBarOF = 13, kBarDrain = 15, kNumBars = 16
+};
+
+struct Unit {
+  int bat, g, u;
+  int head[2];
+  int row0[2];
+  int qpos_max;   // latest global query position held by the CTA, -1 if none
+};
+
+__device__ __forceinline__ Unit decode_unit(const RingParams& p, int idx) {
+  Unit w;
+  const int bg = idx / p.units_per_bg;
+  int r = idx - bg * p.units_per_bg;
+  w.bat = bg / p.G;
+  w.g = bg - w.bat * p.G;
+  const int hp = r % p.pairs_per_g;
+  r /= p.pairs_per_g;
+  // Within one (batch, kv head), launch the latest query positions first: under
+  // a causal mask they carry the most key tiles.
+  const int key = p.P * p.nqq - 1 - r;
+  int qq;
+  if (p.layout == kContiguous) {
+    w.u = key / p.nqq;
+    qq = key - w.u * p.nqq;
+  } else {
+    qq = key / p.P;
+    w.u = key - qq * p.P;
+  }
+  const int hpg = p.H / p.G;
+  if (p.pair_heads) {
+    w.head[0] = w.g * hpg + 2 * hp;
+    w.head[1] = w.head[0] + 1;
+    w.row0[0] = w.row0[1] = qq * 128;
+  } else {
+    w.head[0] = w.head[1] = w.g * hpg + hp;
+    w.row0[0] = 2 * qq * 128;
+    w.row0[1] = w.row0[0] + 128;
+  }
+  w.qpos_max = -1;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (w.row0[i] < p.S) {
+      const int last = min(w.row0[i] + 127, p.S - 1);
+      w.qpos_max = max(w.qpos_max, pos_of(p.layout, p.S, p.P, w.u, last));
+    }
+  }
+  return w;
+}
+
+__device__ __forceinline__ int shard_at(const RingParams& p, int u, int s) {
+  int b = (u - s) % p.P;
+  return b < 0 ? b + p.P : b;
+}
+
+// Key tiles of shard b that some query of the CTA may see (a prefix of the shard).
+__device__ __forceinline__ int kv_tiles(const RingParams& p, int b, int qpos_max) {
+  const int n = visible_prefix(p.layout, p.S, p.P, p.causal, b, 0, p.S, qpos_max);
+  return (n + 127) >> 7;
+}
+
+// TMA box coordinates (innermost first) of 128 rows starting at local row i0
+// of shard u: the tensor maps view [B, N, heads, d] as (d, heads, S, P, B) for
+// the contiguous layout and (d, heads, P, S, B) for the striped one.
+__device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                         int layout, int chunk, int head, int u, int i0,
+                                         int bat) {
+  if (layout == kContiguous)
+    tma_load_5d(dst, map, bar, chunk * 64, head, i0, u, bat);
+  else
+    tma_load_5d(dst, map, bar, chunk * 64, head, u, i0, bat);
+}
+
+__device__ __forceinline__ void record_failure(const RingParams& p, volatile int* abort_flag) {
+  atomicCAS(p.status, 0, static_cast<int>(RA_ERR_TIMEOUT));
+  *abort_flag = 1;
+}
+
+// S = Q K^T for one sub-tile: D/16 MMAs of 128 x 128 x 16, K-major operands in
+// 128-byte-swizzled 64-column chunks.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * Smem<D>::kChunk + (kk & 3) * 32);
+    mma_ss(d_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O += P V for one sub-tile: 8 MMAs of 128 x D x 16; P (bf16, two per TMEM
+// column) from TMEM, V MN-major from shared memory (16 key rows = 2 KiB per MMA,
+// 64-column chunks Smem::kChunk apart).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    mma_ts(d_tmem, p_tmem + kk * 8,
+           smem_desc_sw128(v_smem + kk * 2048, Smem<D>::kChunk, 1024), idesc,
+           (kk > 0 || accumulate) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUtensorMap tq,
+               const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using L = Smem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kNumBars + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Unit w = decode_unit(p, blockIdx.x);
+
+  // Number of key tiles this CTA folds (every role walks the same sequence).
+  int T = 0;
+  for (int s = p.s_begin; s < p.s_end; ++s) T += kv_tiles(p, shard_at(p, w.u, s), w.qpos_max);
+
+  if (T == 0) {
+    // Only in step mode: this shard is invisible to every row of the CTA, so the
+    // state is unchanged — or starts empty.
+    if (p.step_mode && !p.load_state && threadIdx.x < 256) {
+      const int i = threadIdx.x >> 7;
+      const int row = w.row0[i] + (threadIdx.x & 127);
+      if (row < p.S) {
+        const int tok = pos_of(p.layout, p.S, p.P, w.u, row);
+        const size_t md = (static_cast<size_t>(w.bat) * p.H + w.head[i]) * p.N + tok;
+        p.m[md] = -INFINITY;
+        p.z[md] = 0.f;
+        float4* yr = reinterpret_cast<float4*>(
+            p.y + ((static_cast<size_t>(w.bat) * p.N + tok) * p.H + w.head[i]) * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) yr[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(kBarPF + 0), 4);   // one arrival per softmax warp
+    mbar_init(bar(kBarPF + 1), 4);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tensormap(&tq);
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      // loads issued per barrier (for the drain on abort): K/V stages 0 and 1
+      uint32_t nk0 = 0, nk1 = 0, nv0 = 0, nv1 = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(kBarQ), 2 * L::kTile);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_rows(&tq, sbase + L::kQ + i * L::kTile + c * L::kChunk, bar(kBarQ), p.layout, c,
+                   w.head[i], w.u, w.row0[i], w.bat);
+      int t = 0;
+      for (int s = p.s_begin; s < p.s_end && ok; ++s) {
+        const int b = shard_at(p, w.u, s);
+        const int nk = kv_tiles(p, b, w.qpos_max);
+        for (int kt = 0; kt < nk; ++kt, ++t) {
+          const int st = t & 1;
+          const uint32_t n = static_cast<uint32_t>(t >> 1);
+          if (t >= 2 && !bounded_wait(bar(kBarKE + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarKF + st), L::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_rows(&tk, sbase + L::kK + st * L::kTile + c * L::kChunk, bar(kBarKF + st),
+                     p.layout, c, w.g, b, kt * 128, w.bat);
+          if (st) ++nk1; else ++nk0;
+          if (t >= 2 && !bounded_wait(bar(kBarVE + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarVF + st), L::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_rows(&tv, sbase + L::kV + st * L::kTile + c * L::kChunk, bar(kBarVF + st),
+                     p.layout, c, w.g, b, kt * 128, w.bat);
+          if (st) ++nv1; else ++nv0;
+        }
+      }
+      if (!ok) {
+        record_failure(p, abort_flag);
+        bounded_wait(bar(kBarQ), 0, kDrainNs, nullptr);
+        if (nk0) bounded_wait(bar(kBarKF), (nk0 - 1) & 1, kDrainNs, nullptr);
+        if (nk1) bounded_wait(bar(kBarKF + 1), (nk1 - 1) & 1, kDrainNs, nullptr);
+        if (nv0) bounded_wait(bar(kBarVF), (nv0 - 1) & 1, kDrainNs, nullptr);
+        if (nv1) bounded_wait(bar(kBarVF + 1), (nv1 - 1) & 1, kDrainNs, nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t tS0 = tmem, tS1 = tmem + 128;
+      const uint32_t tO0 = tmem + L::kOcol, tO1 = tmem + L::kOcol + D;
+      const uint32_t q0 = sbase + L::kQ, q1 = sbase + L::kQ + L::kTile;
+      bool ok = bounded_wait(bar(kBarQ), 0, p.timeout_ns, abort_flag) &&
+                bounded_wait(bar(kBarKF), 0, p.timeout_ns, abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_qk<D>(tS0, q0, sbase + L::kK);
+        mma_commit(bar(kBarSF + 0));
+        issue_qk<D>(tS1, q1, sbase + L::kK);
+        mma_commit(bar(kBarSF + 1));
+        mma_commit(bar(kBarKE + 0));
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t & 1;
+        const uint32_t ph = static_cast<uint32_t>(t >> 1) & 1;
+        const bool has_next = t + 1 < T;
+        const int st1 = (t + 1) & 1;
+        const uint32_t ph1 = static_cast<uint32_t>((t + 1) >> 1) & 1;
+        const uint32_t vs = sbase + L::kV + st * L::kTile;
+        const uint32_t ks1 = sbase + L::kK + st1 * L::kTile;
+        const bool acc = t > 0 || p.load_state;
+        if (!bounded_wait(bar(kBarVF + st), ph, p.timeout_ns, abort_flag) ||
+            !bounded_wait(bar(kBarPF + 0), t & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_pv<D>(tO0, tS0, vs, acc);
+        if (!has_next) mma_commit(bar(kBarOF + 0));
+        if (has_next) {
+          if (!bounded_wait(bar(kBarKF + st1), ph1, p.timeout_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_qk<D>(tS0, q0, ks1);
+          mma_commit(bar(kBarSF + 0));
+        }
+        if (!bounded_wait(bar(kBarPF + 1), t & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_pv<D>(tO1, tS1, vs, acc);
+        mma_commit(bar(kBarVE + st));
+        if (!has_next) mma_commit(bar(kBarOF + 1));
+        if (has_next) {
+          issue_qk<D>(tS1, q1, ks1);
+          mma_commit(bar(kBarSF + 1));
+          mma_commit(bar(kBarKE + st1));
+        }
+      }
+      if (!ok) {
+        record_failure(p, abort_flag);
+        mma_commit(bar(kBarDrain));
+        bounded_wait(bar(kBarDrain), 0, kDrainNs, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int i = warp >> 2;                 // sub-tile of this group
+    const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int row = w.row0[i] + quarter * 32 + lane;
+    const bool valid = row < p.S;
+    const int qpos = valid ? pos_of(p.layout, p.S, p.P, w.u, row) : -1;
+    const int head = w.head[i];
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + i * 128 + lane_off;
+    const uint32_t tO = tmem + L::kOcol + i * D + lane_off;
+    const size_t md = valid ? (static_cast<size_t>(w.bat) * p.H + head) * p.N + qpos : 0;
+    const size_t yo = valid ? ((static_cast<size_t>(w.bat) * p.N + qpos) * p.H + head) * D : 0;
+    const float c2 = p.scale_log2;
+    float m_run = -INFINITY;   // running max, log2 units
+    float z_run = 0.f;         // running denominator
+
+    if (p.step_mode && p.load_state) {
+      if (valid) {
+        const float mm = p.m[md];
+        m_run = (mm == -INFINITY) ? -INFINITY : mm * kLog2e;
+        z_run = p.z[md];
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t buf[32];
+        if (valid) {
+          const float4* src = reinterpret_cast<const float4*>(p.y + yo + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 f = src[j];
+            buf[4 * j + 0] = __float_as_uint(f.x);
+            buf[4 * j + 1] = __float_as_uint(f.y);
+            buf[4 * j + 2] = __float_as_uint(f.z);
+            buf[4 * j + 3] = __float_as_uint(f.w);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) buf[j] = 0u;
+        }
+        tmem_st_x32(tO + c * 32, buf);
+      }
+      tmem_st_wait();
+    }
+
+    bool ok = true;
+    int t = 0;
+    for (int s = p.s_begin; s < p.s_end && ok; ++s) {
+      const int b = shard_at(p, w.u, s);
+      const int nk = kv_tiles(p, b, w.qpos_max);
+      for (int kt = 0; kt < nk; ++kt, ++t) {
+        const bool got = bounded_wait(bar(kBarSF + i), t & 1, p.timeout_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        float sc[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_x32(tS + c * 32, r);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sc[c * 32 + j] = __uint_as_float(r[j]);
+        }
+        // Causal and shard-tail mask: the visible keys of this tile are a prefix.
+        const int cnt = visible_prefix(p.layout, p.S, p.P, p.causal, b, kt * 128, 128, qpos);
+        if (__any_sync(0xffffffffu, cnt < 128)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= cnt) sc[c] = -INFINITY;
+        }
+        float mx0 = sc[0], mx1 = sc[1], mx2 = sc[2], mx3 = sc[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, sc[c]);
+          mx1 = fmaxf(mx1, sc[c + 1]);
+          mx2 = fmaxf(mx2, sc[c + 2]);
+          mx3 = fmaxf(mx3, sc[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+        const float m_new = fmaxf(m_run, m_tile);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_new > m_run) {
+          if (m_run == -INFINITY) {
+            alpha = 0.f;            // nothing accumulated yet: the state is zero
+          } else {
+            alpha = ex2(m_run - m_new);
+            rescale = true;
+          }
+        }
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        m_run = m_new;
+        float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          sc[c] = ex2(fmaf(sc[c], c2, -m_use));
+          sc[c + 1] = ex2(fmaf(sc[c + 1], c2, -m_use));
+          sc[c + 2] = ex2(fmaf(sc[c + 2], c2, -m_use));
+          sc[c + 3] = ex2(fmaf(sc[c + 3], c2, -m_use));
+          z0 += sc[c];
+          z1 += sc[c + 1];
+          z2 += sc[c + 2];
+          z3 += sc[c + 3];
+        }
+        z_run = z_run * alpha + ((z0 + z1) + (z2 + z3));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(sc[h2 * 64 + 2 * j], sc[h2 * 64 + 2 * j + 1]);
+          tmem_st_x32(tS + h2 * 32, pk);
+        }
+        // Rescale this row's O by alpha before P V of this tile is issued (the
+        // MMA that produced O so far has completed: see the commit order above).
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float a = rescale ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_x32(tO + c * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * a);
+            tmem_st_x32(tO + c * 32, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPF + i));
+      }
+    }
+
+    if (ok) {
+      const bool got = bounded_wait(bar(kBarOF + i), 0, p.timeout_ns, abort_flag);
+      ok = __all_sync(0xffffffffu, got);
+    }
+    if (!ok) {
+      if (lane == 0) record_failure(p, abort_flag);
+    } else {
+      tc_fence_after_sync();
+      if (!p.step_mode) {
+        const float inv = z_run > 0.f ? 1.f / z_run : 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_x32(tO + c * 32, r);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + yo + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]) * inv, __uint_as_float(r[8 * j + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]) * inv, __uint_as_float(r[8 * j + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]) * inv, __uint_as_float(r[8 * j + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]) * inv, __uint_as_float(r[8 * j + 7]) * inv);
+              dst[j] = v;
+            }
+          }
+        }
+        if (valid) p.lse[md] = z_run > 0.f ? (m_run + log2f(z_run)) * kLn2 : -INFINITY;
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_x32(tO + c * 32, r);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(p.y + yo + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+        }
+        if (valid) {
+          p.m[md] = (m_run == -INFINITY) ? -INFINITY : m_run * kLn2;
+          p.z[md] = z_run;
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const RingParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, cudaStream_t st) {
+  const int smem = Smem<D>::kAlloc;
+  static std::atomic<unsigned long long> attr_done{0};   // one bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_done.load() & bit)) {
+    e = cudaFuncSetAttribute(ring_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit);
+  }
+  const long long grid = static_cast<long long>(p.B) * p.G * p.units_per_bg;
+  if (grid <= 0) return cudaSuccess;
+  ring_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int ring_tc_smem_bytes(int D) { return D == 64 ? Smem<64>::kAlloc : Smem<128>::kAlloc; }
+
+cudaError_t launch_ring_tc(const RingParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t st) {
+  return p.D == 64 ? launch_d<64>(p, tq, tk, tv, st) : launch_d<128>(p, tq, tk, tv, st);
+}
+
+}  // namespace ra

@@ -67,42 +67,55 @@ def dense_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
                     heads: Optional[Sequence[int]] = None, max_chunk_elems: int = 1 << 23):
     """O and LSE of plain softmax attention.
 
-    q [B,N,H,d], k/v [B,N,G,d] (fp64 holding the exact input values).
+    q [B,N,H,d], k/v [B,N,G,d]: arrays holding the exact input values (any float
+    dtype; every slice is converted to fp64 before use).
     rows: optional subset of query tokens (original order) to compute.
     heads: optional subset of query heads to compute.
     Returns O [B, R, Hs, d] and LSE [B, Hs, R] (R = len(rows) or N,
     Hs = len(heads) or H).
     """
-    q = np.asarray(q, dtype=np.float64)
-    k = np.asarray(k, dtype=np.float64)
-    v = np.asarray(v, dtype=np.float64)
     B, N, H, d = q.shape
-    G = k.shape[2]
+    rows_ = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    heads_ = list(range(H)) if heads is None else list(heads)
+    q_rows = np.asarray(q)[:, rows_][:, :, heads_]
+    return attention_at(q_rows, rows_, heads_, H, k, v, causal, scale, max_chunk_elems)
+
+
+def attention_at(q_rows: np.ndarray, rows: Sequence[int], heads: Sequence[int], n_heads: int,
+                 k: np.ndarray, v: np.ndarray, causal: bool, scale: Optional[float] = None,
+                 max_chunk_elems: int = 1 << 23):
+    """Attention of given query vectors q_rows [B, R, Hs, d], which sit at token
+    positions `rows` and belong to query heads `heads` (of n_heads), over all N
+    keys of k/v [B, N, G, d]. Returns O [B, R, Hs, d] and LSE [B, Hs, R] in fp64."""
+    B, R, Hs, d = q_rows.shape
+    N, G = k.shape[1], k.shape[2]
     assert k.shape == (B, N, G, d) and v.shape == (B, N, G, d)
-    assert H % G == 0
+    assert n_heads % G == 0
     if scale is None:
         scale = default_scale(d)
-    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
-    heads = list(range(H)) if heads is None else list(heads)
-    R = len(rows)
-    O = np.zeros((B, R, len(heads), d))
-    LSE = np.zeros((B, len(heads), R))
+    rows = np.asarray(rows, dtype=np.int64)
+    O = np.zeros((B, R, Hs, d))
+    LSE = np.zeros((B, Hs, R))
     chunk = max(1, max_chunk_elems // max(N, 1))
     keys = np.arange(N)
     for b in range(B):
+        by_g = {}
         for hi, h in enumerate(heads):
-            g = kv_head_of(h, H, G)
-            K = k[b, :, g, :]
-            V = v[b, :, g, :]
-            for r0 in range(0, R, chunk):
-                rr = rows[r0:r0 + chunk]
-                if causal:
-                    allowed = keys[None, :] <= rr[:, None]
-                else:
-                    allowed = np.ones((len(rr), N), dtype=bool)
-                o, lse = attend_rows(q[b, rr, h, :], K, V, allowed, scale)
-                O[b, r0:r0 + len(rr), hi, :] = o
-                LSE[b, hi, r0:r0 + len(rr)] = lse
+            by_g.setdefault(kv_head_of(h, n_heads, G), []).append(hi)
+        for g, his in by_g.items():
+            K = np.asarray(k[b, :, g, :], dtype=np.float64)
+            V = np.asarray(v[b, :, g, :], dtype=np.float64)
+            for hi in his:
+                for r0 in range(0, R, chunk):
+                    rr = rows[r0:r0 + chunk]
+                    if causal:
+                        allowed = keys[None, :] <= rr[:, None]
+                    else:
+                        allowed = np.ones((len(rr), N), dtype=bool)
+                    qr = np.asarray(q_rows[b, r0:r0 + len(rr), hi, :], dtype=np.float64)
+                    o, lse = attend_rows(qr, K, V, allowed, scale)
+                    O[b, r0:r0 + len(rr), hi, :] = o
+                    LSE[b, hi, r0:r0 + len(rr)] = lse
     return O, LSE
 
 

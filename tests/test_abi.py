@@ -1,0 +1,105 @@
+"""The C ABI on the CPU: the library builds, loads, exports every symbol the
+header declares, checks its arguments before touching the GPU, and its host
+shard map is bit-exact against the oracle's."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from online_softmax_merge_gb300 import _lib
+from online_softmax_merge_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ringattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _lib.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|ra_status|int32_t)\s+(\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declarations_match_binding():
+    assert _declared() == sorted(_lib.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert lib.ring_attn_version() == 100
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.ra_status_str(code).decode() == name
+
+
+def _pr(**kw):
+    base = dict(batch=1, seqlen=256, heads=4, kv_heads=2, head_dim=128, P=2, causal=1, layout=0,
+                scale=0.0)
+    base.update(kw)
+    return _lib.RaProblem(**base)
+
+
+FAKE = ctypes.c_void_p(0x10000)      # aligned, never dereferenced: checks fail first
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(seqlen=255), _lib.RA_ERR_INVALID_ARG),          # N % P != 0
+    (dict(heads=3), _lib.RA_ERR_INVALID_ARG),             # H % G != 0
+    (dict(batch=0), _lib.RA_ERR_INVALID_ARG),
+    (dict(P=0), _lib.RA_ERR_INVALID_ARG),
+    (dict(P=512), _lib.RA_ERR_INVALID_ARG),               # P > N
+    (dict(layout=2), _lib.RA_ERR_INVALID_ARG),
+    (dict(causal=2), _lib.RA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), _lib.RA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _lib.RA_ERR_INVALID_ARG),
+    (dict(head_dim=96), _lib.RA_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_bad_problems_before_any_launch(lib, bad, code):
+    pr = _pr(**bad)
+    assert lib.ring_attn_fwd(ctypes.byref(pr), FAKE, FAKE, FAKE, FAKE, FAKE, None) == code
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    pr = _pr()
+    assert lib.ring_attn_fwd(None, FAKE, FAKE, FAKE, FAKE, FAKE, None) == _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_fwd(ctypes.byref(pr), None, FAKE, FAKE, FAKE, FAKE, None) == \
+        _lib.RA_ERR_INVALID_ARG
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.ring_attn_fwd(ctypes.byref(pr), FAKE, odd, FAKE, FAKE, FAKE, None) == \
+        _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_step(ctypes.byref(pr), 2, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              None) == _lib.RA_ERR_INVALID_ARG        # s >= P
+    assert lib.ring_attn_merge(0, 1, 8, 1, 128, FAKE, FAKE, FAKE, FAKE, None) == \
+        _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_merge(2, 1, 8, 1, 80, FAKE, FAKE, FAKE, FAKE, None) == \
+        _lib.RA_ERR_UNSUPPORTED
+    assert lib.ring_attn_tile_classes(ctypes.byref(pr), 2, 0, FAKE, None) == \
+        _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_selftest_timeout(0, None) == _lib.RA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("N,P", [(8, 4), (12, 3), (1024, 16), (96, 96), (7, 1)])
+def test_host_shard_map_bit_exact_vs_oracle(lib, layout, N, P):
+    from oracle import shardmap as OS
+    import online_softmax_merge_gb300 as ra
+    got = ra.shard_map(layout, N, P)
+    want = OS.shard_map(layout, N, P)
+    assert got == tuple(want) or list(got) == list(want)
+
+
+def test_host_shard_map_rejects_bad_sizes(lib):
+    arr = (ctypes.c_int32 * 10)()
+    assert lib.ring_attn_shard_map(0, 10, 3, arr, arr, arr) == _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_shard_map(5, 10, 2, arr, arr, arr) == _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_shard_map(0, 10, 2, None, arr, arr) == _lib.RA_ERR_INVALID_ARG

@@ -1,0 +1,76 @@
+"""Parity at the five measured configurations, in the launch configuration the
+bench times (one ring_attn_fwd call). The 1024-token case is checked on every
+row; the large ones on sampled rows -- the first and last row of shards plus
+seeded random rows -- each computed exactly by the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import TOL_LSE, TOL_O, compare_full, compare_rows, sample_rows
+from online_softmax_merge_gb300.inputs import WORKLOADS, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+ra = pytest.importorskip("online_softmax_merge_gb300")
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+def _fwd(w, q, k, v, layout=None):
+    o, lse = ra.fwd(q, k, v, w.P, layout or w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    return o, lse
+
+
+def test_c1_full():
+    w = WORKLOADS["c1"]
+    q, k, v = (t.to(DEV) for t in make_qkv(w))
+    o, lse = _fwd(w, q, k, v)
+    eo, el = compare_full(o, lse, q, k, v, w.causal)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+
+
+def test_c2_sampled():
+    w = WORKLOADS["c2"]
+    q, k, v = make_qkv(w, device=DEV)
+    o, lse = _fwd(w, q, k, v)
+    rows = sample_rows(w.layout, w.seqlen, w.P, 16, seed=2)
+    eo, el = compare_rows(o, lse, q, k, v, True, rows, range(w.heads))
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+
+
+def test_c3_striped_and_contiguous_on_same_tensors():
+    w = WORKLOADS["c3"]
+    q, k, v = make_qkv(w, device=DEV)
+    o_s, l_s = _fwd(w, q, k, v, "striped")
+    rows = sample_rows("striped", w.seqlen, w.P, 8, seed=3)
+    heads = [0, 5, 10, 15, 16, 21, 26, 31]
+    eo, el = compare_rows(o_s, l_s, q, k, v, True, rows, heads)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+    o_c, l_c = _fwd(w, q, k, v, "contiguous")
+    rows_c = sample_rows("contiguous", w.seqlen, w.P, 8, seed=4)
+    eo, el = compare_rows(o_c, l_c, q, k, v, True, rows_c, heads)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+    assert float((o_s.float() - o_c.float()).abs().max()) <= TOL_O
+    assert float((l_s - l_c).abs().max()) <= TOL_LSE
+
+
+def test_c4_sampled():
+    w = WORKLOADS["c4"]
+    q, k, v = make_qkv(w, device=DEV)
+    o, lse = _fwd(w, q, k, v)
+    rows = sample_rows(w.layout, w.seqlen, w.P, 8, seed=5)
+    eo, el = compare_rows(o, lse, q, k, v, True, rows, [0, 3, 9, 14, 18, 23, 25, 31])
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+    # the stressed key rows (x8) are where the max rescale works hardest
+    assert torch.isfinite(lse).all()
+
+
+def test_c5_sampled():
+    w = WORKLOADS["c5"]
+    q, k, v = make_qkv(w, device=DEV)
+    o, lse = _fwd(w, q, k, v)
+    rows = sample_rows(w.layout, w.seqlen, w.P, 8, seed=6, shards=[0, 1, 31, 62, 63])
+    eo, el = compare_rows(o, lse, q, k, v, True, rows, [0, 13, 22, 31])
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+    assert torch.isfinite(lse).all()

@@ -1,0 +1,141 @@
+"""GPU parity of the fused ring forward (ring_attn_fwd) against the fp64 oracle,
+at sizes the oracle computes in full: several 128-row tiles, ragged shard tails,
+both layouts, causal and not, GQA and MHA, d in {64, 128}, and the degenerate
+cases of the method."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import TOL_LSE, TOL_O, compare_full, host32
+from online_softmax_merge_gb300.inputs import Workload, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+ra = pytest.importorskip("online_softmax_merge_gb300")
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+def _run(w: Workload, scale=0.0):
+    q, k, v = make_qkv(w)
+    q, k, v = q.to(DEV), k.to(DEV), v.to(DEV)
+    o, lse = ra.fwd(q, k, v, w.P, w.layout, w.causal, scale)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    return q, k, v, o, lse
+
+
+CASES = [
+    # name, B, N, H, G, d, P, layout, causal
+    ("gqa-contig-causal-tail", 1, 4 * (3 * 128 + 40), 4, 2, 128, 4, "contiguous", True),
+    ("gqa-striped-causal-tail", 1, 4 * (3 * 128 + 40), 4, 2, 128, 4, "striped", True),
+    ("gqa-contig-full-tail", 1, 2 * (2 * 128 + 72), 4, 2, 128, 2, "contiguous", False),
+    ("gqa-striped-full", 2, 8 * 64, 8, 2, 128, 8, "striped", False),
+    ("mha-odd-tiles", 1, 3 * (5 * 128 + 8), 3, 3, 128, 3, "contiguous", True),
+    ("gqa3-striped", 1, 2 * (3 * 128 + 1), 6, 2, 128, 2, "striped", True),
+    ("d64-contig-causal", 2, 4 * 200, 4, 1, 64, 4, "contiguous", True),
+    ("d64-striped-causal", 1, 4 * 300, 2, 2, 64, 4, "striped", True),
+    ("p1-plain", 1, 700, 2, 1, 128, 1, "contiguous", True),
+    ("s1-every-token-a-shard", 1, 64, 2, 1, 128, 64, "striped", True),
+    ("s1-contig", 1, 48, 2, 2, 64, 48, "contiguous", True),
+    ("tiny", 1, 5, 2, 2, 128, 1, "contiguous", False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fwd_matches_oracle(case):
+    name, B, N, H, G, d, P, layout, causal = case
+    w = Workload(name, B, N, H, G, d, P, layout, causal, seed=100 + CASES.index(case))
+    q, k, v, o, lse = _run(w)
+    eo, el = compare_full(o, lse, q, k, v, causal)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+
+
+def test_contiguous_equals_striped_on_same_tensors():
+    w = Workload("cs", 1, 8 * 192, 4, 2, 128, 8, "contiguous", True, seed=5)
+    q, k, v, o1, l1 = _run(w)
+    o2, l2 = ra.fwd(q, k, v, w.P, "striped", True)
+    torch.cuda.synchronize()
+    assert float((o1.float() - o2.float()).abs().max()) <= TOL_O
+    assert float((l1 - l2).abs().max()) <= TOL_LSE
+
+
+def test_p_invariance_and_p1_is_plain_attention():
+    w = Workload("pinv", 1, 1024, 4, 2, 128, 1, "contiguous", True, seed=6)
+    q, k, v, o1, l1 = _run(w)
+    for P in (2, 4, 8):
+        for layout in ("contiguous", "striped"):
+            o2, l2 = ra.fwd(q, k, v, P, layout, True)
+            torch.cuda.synchronize()
+            assert float((o1.float() - o2.float()).abs().max()) <= TOL_O
+            assert float((l1 - l2).abs().max()) <= TOL_LSE
+
+
+def test_worked_example_zero_padded():
+    """The chapter's printed example (d = 1, raw products as scores), padded to
+    d = 64 with zeros and run with scale 1."""
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_example.json")))
+    q = torch.zeros((1, 4, 1, 64), dtype=torch.bfloat16)
+    k = torch.zeros_like(q)
+    v = torch.zeros_like(q)
+    q[0, :, 0, 0] = torch.tensor(g["Q"], dtype=torch.bfloat16)
+    k[0, :, 0, 0] = torch.tensor(g["K"], dtype=torch.bfloat16)
+    v[0, :, 0, 0] = torch.tensor(g["V"], dtype=torch.bfloat16)
+    o, lse = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), g["P"], "contiguous", False, scale=1.0)
+    torch.cuda.synchronize()
+    got = host32(o)[0, :, 0, 0]
+    want = np.array(g["outputs"]["values"])
+    # bf16 rounding of P (2^-9 relative) weighted by |V| <= 40, plus bf16 output rounding
+    tol = 2.0 ** -8 * 40 + 2.0 ** -8 * np.abs(want)
+    assert np.all(np.abs(got - want) <= tol), (got, want)
+    lse_want = [math.log(sum(math.exp(qq * kk) for kk in g["K"])) for qq in g["Q"]]
+    assert np.abs(host32(lse)[0, 0] - np.array(lse_want)).max() <= TOL_LSE
+    assert np.all(host32(o)[0, :, 0, 1:] == 0)
+
+
+def test_zero_queries_give_mean_of_visible_values():
+    w = Workload("q0", 1, 4 * 160, 2, 1, 128, 4, "striped", True, seed=7)
+    q, k, v = make_qkv(w)
+    q = torch.zeros_like(q)
+    o, lse = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, True)
+    torch.cuda.synchronize()
+    vv = v[0, :, 0].double()
+    mean = torch.cumsum(vv, 0) / torch.arange(1, w.seqlen + 1, dtype=torch.float64)[:, None]
+    assert float((o[0, :, 0].cpu().double() - mean).abs().max()) <= TOL_O
+    want_lse = torch.log(torch.arange(1, w.seqlen + 1, dtype=torch.float64))
+    assert float((lse[0, 0].cpu().double() - want_lse).abs().max()) <= TOL_LSE
+
+
+def test_constant_values_and_first_token():
+    w = Workload("v1", 1, 2 * 256, 4, 2, 128, 2, "contiguous", True, seed=8)
+    q, k, v = make_qkv(w)
+    ones = torch.ones_like(v)
+    o, lse = ra.fwd(q.to(DEV), k.to(DEV), ones.to(DEV), w.P, w.layout, True)
+    torch.cuda.synchronize()
+    # rows sum to 1 (P is rounded to bf16 for the MMA, the denominator is not)
+    assert float((o.float() - 1.0).abs().max()) <= TOL_O
+    o, lse = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, True)
+    torch.cuda.synchronize()
+    assert torch.equal(o[:, 0].cpu(), v[:, 0].repeat_interleave(2, dim=1))   # token 0 sees itself
+    s00 = (q[0, 0].double() * k[0, 0].repeat_interleave(2, dim=0).double()).sum(-1) / math.sqrt(128)
+    assert float((lse[0, :, 0].cpu().double() - s00).abs().max()) <= TOL_LSE
+
+
+def test_large_logits_stress():
+    # keys scaled x8 on 1% of rows (like the 131072-token stress configuration)
+    w = Workload("stress", 1, 4 * 256, 4, 2, 128, 4, "contiguous", True, seed=9,
+                 stress_frac=0.05, stress_factor=8.0)
+    q, k, v, o, lse = _run(w)
+    eo, el = compare_full(o, lse, q, k, v, True)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+
+
+def test_repeated_calls_are_deterministic():
+    w = Workload("det", 1, 2 * 384, 4, 2, 128, 2, "striped", True, seed=10)
+    q, k, v, o1, l1 = _run(w)
+    o2, l2 = ra.fwd(q, k, v, w.P, w.layout, True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
