@@ -1,0 +1,420 @@
+"""Benchmark of the ring-attention forward on GB300 (one JSON line on stdout).
+
+Default workload: B=2, N=131072, 32 query heads over 8 KV heads, d=128, P=16
+contiguous virtual shards, causal, bf16 N(0,1) inputs with 1% of key rows x8.
+One step = one ring_attn_fwd call (shard maps, causal tile skip, ring visit
+order, QK^T, online softmax, PV and the final O = y/z, LSE, all in one kernel),
+with inputs resident in HBM. Also measured in the same run:
+  * e2e: the same step through the C ABI with pinned HOST buffers, the host->device
+    copy of Q, K, V and the device->host copy of O, LSE inside the timed region;
+  * merge: ring_attn_merge over n=8 per-shard partials of a B=1, N=32768, H=32,
+    d=128 problem (HBM-bound), as GB/s against the measured copy bandwidth;
+  * cpu_baseline: the fp64 CPU oracle on a bounded sample of query rows.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--impl ours|reference]
+
+With --gpus N > 1 (torch.distributed.run, one process per GPU) every rank runs
+an independent replica of the workload (weak scaling; no collective on the data
+path); value = total FLOPs of all ranks / slowest rank's time.
+--impl reference times the fp64 CPU oracle (the only reference this method has)
+on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from online_softmax_merge_gb300 import replicas  # noqa: E402
+from online_softmax_merge_gb300.inputs import WORKLOAD_TEXT, WORKLOADS, make_merge_inputs, make_qkv  # noqa: E402
+
+METRIC = "ring-attn fwd TFLOP/s (causal-adj) & % GB300 BF16 tensor peak; tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+KERNEL_SOURCES = {
+    "ring_tc_kernel": ["ring_tc.cu", "ptx.cuh", "shardmap.cuh"],
+    "merge_kernel": ["merge.cu"],
+}
+
+
+def source_sha(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "online_softmax_merge_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(key: str):
+    """Per-launch DRAM bytes (read + write) of a kernel from the committed ncu
+    summary profiles/traffic.json, or None when the kernel's sources changed
+    since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f).get(key)
+    except (OSError, ValueError):
+        return None
+    if not entry or entry.get("source_sha") != source_sha(key.split(":")[0]):
+        return None
+    return entry.get("bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        load = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle
+def oracle_sample_rate(q, k, v, w, seconds: float, seed: int = 0):
+    """Run the fp64 CPU oracle on seeded random query rows of the workload until
+    `seconds` have passed; return (causal-adjusted TFLOP/s, tokens/s, rows, s)."""
+    from oracle.attention import attention_at
+    rng = np.random.default_rng(seed)
+    heads = [0, w.heads // 3, (2 * w.heads) // 3, w.heads - 1]
+    flops = 0.0
+    n_rows = 0
+    # slices converted to exact fp32 once (untimed), per (batch, kv head) in use
+    G, H = w.kv_heads, w.heads
+    prepared = {}
+    for h in heads:
+        g = (h * G) // H
+        if (0, g) not in prepared:
+            prepared[(0, g)] = (k[0:1, :, g:g + 1].float().cpu().numpy(),
+                                v[0:1, :, g:g + 1].float().cpu().numpy())
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        h = heads[n_rows % len(heads)]
+        g = (h * G) // H
+        kk, vv = prepared[(0, g)]
+        rows = np.sort(rng.integers(0, w.seqlen, 4))
+        qr = q[0:1, torch.as_tensor(rows, device=q.device)][:, :, h:h + 1].float().cpu().numpy()
+        attention_at(qr, rows, [0], 1, kk, vv, w.causal)
+        for t in rows:
+            flops += 4.0 * w.head_dim * ((t + 1) if w.causal else w.seqlen)
+        n_rows += len(rows)
+    dt = time.perf_counter() - t0
+    tflops = flops / dt / 1e12
+    # tokens/s of the full workload at this rate: FLOPs per token = total / (B*N)
+    tok_s = tflops * 1e12 / (w.causal_flops() / (w.batch * w.seqlen))
+    return tflops, tok_s, n_rows, dt
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [x.get("num_threads", 0) for x in threadpool_info() if x.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args, w):
+    """The fp64 CPU oracle as the reference arm: each step is a bounded sample."""
+    info = replicas.rank_info()
+    if not info.is_main:
+        return 0
+    q, k, v = make_qkv(w, device="cpu")
+    per_step = []
+    rates = []
+    for i in range(args.warmup + args.steps):
+        tf, tok, rows, dt = oracle_sample_rate(q, k, v, w, args.ref_seconds, seed=i)
+        if i >= args.warmup:
+            per_step.append(dt)
+            rates.append((tf, tok, rows))
+    tflops = statistics.mean(r[0] for r in rates)
+    tok_s = statistics.mean(r[1] for r in rates)
+    rows = sum(r[2] for r in rates)
+    cores = oracle_threads()
+    sample = (f"{rows} seeded random query rows of batch 0, heads 0/{w.heads // 3}/"
+              f"{(2 * w.heads) // 3}/{w.heads - 1}, ~{args.ref_seconds:.0f} s per step, "
+              "exact fp64 rows; FLOPs counted causal-adjusted")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_obj(w, args), "tokens_per_s": tok_s,
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_obj(w, args):
+    return {"workload": f"{w.name}: {WORKLOAD_TEXT.get(w.name, '')}", "batch": w.batch,
+            "seqlen": w.seqlen, "heads": w.heads, "kv_heads": w.kv_heads,
+            "head_dim": w.head_dim, "P": w.P, "layout": w.layout, "causal": w.causal,
+            "l2": "inputs larger than L2 (no flush needed)",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def time_launches(fn, steps, stream):
+    """Per-launch durations (ms) with CUDA events on the launching stream."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_ours(args, w):
+    import online_softmax_merge_gb300 as ra
+
+    info = replicas.rank_info()
+    torch.cuda.set_device(info.local_rank)
+    dev = torch.device("cuda", info.local_rank)
+    replicas.init(info, "nccl")
+    peaks, peaks_src = load_peaks()
+    ra.load()
+
+    q, k, v = make_qkv(w, device=dev)
+    o = torch.empty((w.batch, w.seqlen, w.heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.batch, w.heads, w.seqlen), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ra.fwd(q, k, v, w.P, w.layout, w.causal, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ra.last_error(dev) != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    # ---- timed region: K steps, inputs resident in HBM
+    replicas.barrier(info)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(info.local_rank) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        launch_ms = []
+        evs = []
+        for _ in range(args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            evs.append((a, b))
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    replicas.barrier(info)
+    elapsed_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    if ra.last_error(dev) != 0:
+        raise RuntimeError("device-side wait timed out in the timed region")
+    slowest_ms = replicas.max_over_ranks(info, elapsed_ms, device=dev)
+    ms_per_step = slowest_ms / args.steps
+    flops_step = w.causal_flops()
+    value = info.world * flops_step * args.steps / (slowest_ms * 1e-3) / 1e12
+    tokens_s = info.world * w.batch * w.seqlen * args.steps / (slowest_ms * 1e-3)
+
+    # ---- roofline of the forward kernel: algorithmic FLOPs / mean launch time
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    mean_launch_s = statistics.mean(launch_ms) * 1e-3
+    achieved = flops_step / mean_launch_s / 1e12
+    traffic = load_traffic(f"ring_tc_kernel:{w.name}")
+
+    # ---- e2e through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True).copy_(q)
+        hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True).copy_(k)
+        hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            ra.fwd(dq, dk, dv, w.P, w.layout, w.causal, out=o, lse=lse)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        replicas.barrier(info)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = replicas.max_over_ranks(info, a.elapsed_time(b), device=dev)
+        h2d = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
+        d2h = o.numel() * 2 + lse.numel() * 4
+        e2e = {"value": info.world * flops_step * e2e_steps / (e_ms * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "ms_per_step": e_ms / e2e_steps}
+        del hq, hk, hv, ho, hl, dq, dk, dv
+
+    # ---- merge kernel (HBM-bound) on n=8 per-shard partials of a 32768-token problem
+    merge = None
+    if not args.no_merge:
+        n, mB, mN, mH, md = 8, 1, 32768, 32, 128
+        o_p, l_p = make_merge_inputs(n, mB, mN, mH, md, device=dev, seed=3)
+        mo = torch.empty((mB, mN, mH, md), dtype=torch.bfloat16, device=dev)
+        ml = torch.empty((mB, mH, mN), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            ra.merge(o_p, l_p, out=mo, lse=ml)
+        ms = time_launches(lambda: ra.merge(o_p, l_p, out=mo, lse=ml), max(5, args.steps), stream)
+        mbytes = n * mB * mH * mN * (4 * md + 4) + mB * mH * mN * (2 * md + 4)
+        gbs = mbytes / (statistics.mean(ms) * 1e-3) / 1e9
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        merge = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                 "traffic": load_traffic("merge_kernel:n8_B1_N32768_H32_d128"),
+                 "algorithmic_bytes": mbytes, "ms": statistics.mean(ms),
+                 "workload": "n=8 parts, B=1, N=32768, H=32, d=128 fp32 partials -> bf16"}
+        del o_p, l_p, mo, ml
+
+    # ---- the oracle on the host cores (rank 0 only)
+    cpu = None
+    if info.is_main and not args.no_cpu_baseline:
+        tf, tok, rows, dt = oracle_sample_rate(q, k, v, w, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{rows} seeded random query rows (batch 0, 4 heads) of the same "
+                         f"workload, exact fp64, {dt:.1f} s; FLOPs counted causal-adjusted",
+               "tokens_per_s": tok}
+
+    if info.is_main:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": info.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_obj(w, args),
+            "tokens_per_s": tokens_s, "pct_bf16_peak": 100.0 * value / (info.world * peak_tf),
+            "flops_per_step": flops_step,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
+                         "peak_source": f"{peaks_src} bf16 burst",
+                         "kernel": "ring_tc_kernel<128>", "launch_ms": statistics.mean(launch_ms)},
+            "merge_roofline": merge,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    replicas.shutdown(info)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="c4", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layout", default=None, choices=[None, "contiguous", "striped"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-merge", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    w = WORKLOADS[args.config]
+    if args.layout:
+        w = w.with_(layout=args.layout)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -119,7 +119,8 @@ def test_finalize_matches_oracle():
     o, lse = ra.finalize((m.to(DEV), z.to(DEV), y.to(DEV)))
     torch.cuda.synchronize()
     Ow, Lw = OM.finalize(m.double().numpy(), z.double().numpy(), y.double().numpy())
-    assert np.abs(host32(o) - Ow).max() <= TOL_O
+    # |O| reaches ~20 here: the bound is bf16 rounding of the output (half an ulp)
+    assert np.all(np.abs(host32(o) - Ow) <= 2.0 ** -8 * np.abs(Ow) + 1e-6)
     fin = np.isfinite(Lw)
     got = host32(lse)
     assert np.array_equal(np.isfinite(got), fin)
