@@ -51,8 +51,8 @@ def test_c3_striped_and_contiguous_on_same_tensors():
     rows_c = sample_rows("contiguous", w.seqlen, w.P, 8, seed=4)
     eo, el = compare_rows(o_c, l_c, q, k, v, True, rows_c, heads)
     assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
-    assert float((o_s.float() - o_c.float()).abs().max()) <= TOL_O
-    assert float((l_s - l_c).abs().max()) <= TOL_LSE
+    assert float((o_s.float() - o_c.float()).abs().max()) <= 2 * TOL_O
+    assert float((l_s - l_c).abs().max()) <= 2 * TOL_LSE
 
 
 def test_c4_sampled():

@@ -54,13 +54,15 @@ def test_fwd_matches_oracle(case):
     assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
 
 
+# Two GPU results are each within TOL of the exact value, so within 2 TOL of
+# each other (two bf16 roundings of nearly equal values can differ by an ulp).
 def test_contiguous_equals_striped_on_same_tensors():
     w = Workload("cs", 1, 8 * 192, 4, 2, 128, 8, "contiguous", True, seed=5)
     q, k, v, o1, l1 = _run(w)
     o2, l2 = ra.fwd(q, k, v, w.P, "striped", True)
     torch.cuda.synchronize()
-    assert float((o1.float() - o2.float()).abs().max()) <= TOL_O
-    assert float((l1 - l2).abs().max()) <= TOL_LSE
+    assert float((o1.float() - o2.float()).abs().max()) <= 2 * TOL_O
+    assert float((l1 - l2).abs().max()) <= 2 * TOL_LSE
 
 
 def test_p_invariance_and_p1_is_plain_attention():
@@ -70,8 +72,8 @@ def test_p_invariance_and_p1_is_plain_attention():
         for layout in ("contiguous", "striped"):
             o2, l2 = ra.fwd(q, k, v, P, layout, True)
             torch.cuda.synchronize()
-            assert float((o1.float() - o2.float()).abs().max()) <= TOL_O
-            assert float((l1 - l2).abs().max()) <= TOL_LSE
+            assert float((o1.float() - o2.float()).abs().max()) <= 2 * TOL_O
+            assert float((l1 - l2).abs().max()) <= 2 * TOL_LSE
 
 
 def test_worked_example_zero_padded():
