@@ -15,7 +15,8 @@
 //  * warp 9 (TMA producer) loads both Q sub-tiles once, then streams 128-key K and
 //    V tiles of the visited shards through two shared-memory stages each, in the
 //    ring order, skipping key tiles that no query of the CTA may see;
-//  * warp 8 issues the tcgen05 MMAs from one thread: S_i = Q_i K^T into TMEM
+//  * warp 8 issues the tcgen05 MMAs (one elected lane of a warp-uniform loop):
+//    S_i = Q_i K^T into TMEM
 //    (fp32, 128 columns per sub-tile) and O_i += P_i V with P_i read from TMEM;
 //  * warps 0-3 / 4-7 are the softmax groups of sub-tile 0 / 1: one thread per
 //    query row reads its S row from TMEM, applies the causal / tail mask, updates
@@ -141,29 +142,30 @@ __device__ __forceinline__ void record_failure(const RingParams& p, volatile int
 }
 
 // S = Q K^T for one sub-tile: D/16 MMAs of 128 x 128 x 16, K-major operands in
-// 128-byte-swizzled 64-column chunks.
+// 128-byte-swizzled 64-column chunks. q_desc / k_desc describe the tile bases;
+// the k-th MMA reads 16 columns further on (+32 B inside a 128-B row, a new
+// 64-column chunk every four), i.e. a constant added to the address field.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = static_cast<uint32_t>((kk >> 2) * Smem<D>::kChunk + (kk & 3) * 32);
-    mma_ss(d_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024),
-           idesc, kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * Smem<D>::kChunk + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 // O += P V for one sub-tile: 8 MMAs of 128 x D x 16; P (bf16, two per TMEM
 // column) from TMEM, V MN-major from shared memory (16 key rows = 2 KiB per MMA,
-// 64-column chunks Smem::kChunk apart).
+// 64-column chunks Smem::kChunk apart, which v_desc carries as its leading
+// byte offset).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    mma_ts(d_tmem, p_tmem + kk * 8,
-           smem_desc_sw128(v_smem + kk * 2048, Smem<D>::kChunk, 1024), idesc,
+    mma_ts(d_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
            (kk > 0 || accumulate) ? 1u : 0u);
   }
 }
@@ -284,19 +286,32 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // The whole warp runs the loop and the waits (warp-uniform control flow and
+    // operands); one elected lane issues each group of MMAs and commits. A loop
+    // run by a single lane issues MMAs far slower than the tensor core executes
+    // them.
+    {
       const uint32_t tS0 = tmem, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + L::kOcol, tO1 = tmem + L::kOcol + D;
-      const uint32_t q0 = sbase + L::kQ, q1 = sbase + L::kQ + L::kTile;
-      bool ok = bounded_wait(bar(kBarQ), 0, p.timeout_ns, abort_flag) &&
-                bounded_wait(bar(kBarKF), 0, p.timeout_ns, abort_flag);
+      // Shared-memory descriptors of every tile base, computed once.
+      const uint64_t dq0 = smem_desc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(sbase + L::kQ + L::kTile, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t dk1 = smem_desc_sw128(sbase + L::kK + L::kTile, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sbase + L::kV, L::kChunk, 1024);
+      const uint64_t dv1 = smem_desc_sw128(sbase + L::kV + L::kTile, L::kChunk, 1024);
+      bool ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarQ), 0, p.timeout_ns, abort_flag) &&
+                                        bounded_wait(bar(kBarKF), 0, p.timeout_ns, abort_flag));
       if (ok) {
         tc_fence_after_sync();
-        issue_qk<D>(tS0, q0, sbase + L::kK);
-        mma_commit(bar(kBarSF + 0));
-        issue_qk<D>(tS1, q1, sbase + L::kK);
-        mma_commit(bar(kBarSF + 1));
-        mma_commit(bar(kBarKE + 0));
+        if (elect_one()) {
+          issue_qk<D>(tS0, dq0, dk0);
+          mma_commit(bar(kBarSF + 0));
+          issue_qk<D>(tS1, dq1, dk0);
+          mma_commit(bar(kBarSF + 1));
+          mma_commit(bar(kBarKE + 0));
+        }
+        __syncwarp();
       }
       for (int t = 0; t < T && ok; ++t) {
         const int st = t & 1;
@@ -304,43 +319,53 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
         const bool has_next = t + 1 < T;
         const int st1 = (t + 1) & 1;
         const uint32_t ph1 = static_cast<uint32_t>((t + 1) >> 1) & 1;
-        const uint32_t vs = sbase + L::kV + st * L::kTile;
-        const uint32_t ks1 = sbase + L::kK + st1 * L::kTile;
+        const uint64_t vs = st ? dv1 : dv0;
+        const uint64_t ks1 = st1 ? dk1 : dk0;
         const bool acc = t > 0 || p.load_state;
-        if (!bounded_wait(bar(kBarVF + st), ph, p.timeout_ns, abort_flag) ||
-            !bounded_wait(bar(kBarPF + 0), t & 1, p.timeout_ns, abort_flag)) {
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarVF + st), ph, p.timeout_ns, abort_flag) &&
+                                     bounded_wait(bar(kBarPF + 0), t & 1, p.timeout_ns, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        issue_pv<D>(tO0, tS0, vs, acc);
-        if (!has_next) mma_commit(bar(kBarOF + 0));
+        if (elect_one()) {
+          issue_pv<D>(tO0, tS0, vs, acc);
+          if (!has_next) mma_commit(bar(kBarOF + 0));
+        }
+        __syncwarp();
         if (has_next) {
-          if (!bounded_wait(bar(kBarKF + st1), ph1, p.timeout_ns, abort_flag)) {
+          if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarKF + st1), ph1, p.timeout_ns, abort_flag))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          issue_qk<D>(tS0, q0, ks1);
-          mma_commit(bar(kBarSF + 0));
+          if (elect_one()) {
+            issue_qk<D>(tS0, dq0, ks1);
+            mma_commit(bar(kBarSF + 0));
+          }
+          __syncwarp();
         }
-        if (!bounded_wait(bar(kBarPF + 1), t & 1, p.timeout_ns, abort_flag)) {
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 1), t & 1, p.timeout_ns, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        issue_pv<D>(tO1, tS1, vs, acc);
-        mma_commit(bar(kBarVE + st));
-        if (!has_next) mma_commit(bar(kBarOF + 1));
-        if (has_next) {
-          issue_qk<D>(tS1, q1, ks1);
-          mma_commit(bar(kBarSF + 1));
-          mma_commit(bar(kBarKE + st1));
+        if (elect_one()) {
+          issue_pv<D>(tO1, tS1, vs, acc);
+          mma_commit(bar(kBarVE + st));
+          if (!has_next) mma_commit(bar(kBarOF + 1));
+          if (has_next) {
+            issue_qk<D>(tS1, dq1, ks1);
+            mma_commit(bar(kBarSF + 1));
+            mma_commit(bar(kBarKE + st1));
+          }
         }
+        __syncwarp();
       }
       if (!ok) {
-        record_failure(p, abort_flag);
-        mma_commit(bar(kBarDrain));
+        if (lane == 0) record_failure(p, abort_flag);
+        if (elect_one()) mma_commit(bar(kBarDrain));
+        __syncwarp();
         bounded_wait(bar(kBarDrain), 0, kDrainNs, nullptr);
       }
     }
@@ -359,7 +384,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     const size_t md = valid ? (static_cast<size_t>(w.bat) * p.H + head) * p.N + qpos : 0;
     const size_t yo = valid ? ((static_cast<size_t>(w.bat) * p.N + qpos) * p.H + head) * D : 0;
     const float c2 = p.scale_log2;
-    float m_run = -INFINITY;   // running max, log2 units
+    float m_run = -INFINITY;   // running max of the scaled scores, log2 units
     float z_run = 0.f;         // running denominator
 
     if (p.step_mode && p.load_state) {
@@ -403,12 +428,11 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
         }
         tc_fence_after_sync();
         float sc[128];
+        {
+          uint32_t r[128];
+          tmem_ld_x128(tS, r);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_x32(tS + c * 32, r);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sc[c * 32 + j] = __uint_as_float(r[j]);
+          for (int j = 0; j < 128; ++j) sc[j] = __uint_as_float(r[j]);
         }
         // Causal and shard-tail mask: the visible keys of this tile are a prefix.
         const int cnt = visible_prefix(p.layout, p.S, p.P, p.causal, b, kt * 128, 128, qpos);
@@ -417,41 +441,50 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
           for (int c = 0; c < 128; ++c)
             if (c >= cnt) sc[c] = -INFINITY;
         }
-        float mx0 = sc[0], mx1 = sc[1], mx2 = sc[2], mx3 = sc[3];
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, sc[c]);
-          mx1 = fmaxf(mx1, sc[c + 1]);
-          mx2 = fmaxf(mx2, sc[c + 2]);
-          mx3 = fmaxf(mx3, sc[c + 3]);
+        for (int c = 0; c < 128; c += 8) {
+          mx0 = fmax3(mx0, sc[c], sc[c + 1]);
+          mx1 = fmax3(mx1, sc[c + 2], sc[c + 3]);
+          mx2 = fmax3(mx2, sc[c + 4], sc[c + 5]);
+          mx3 = fmax3(mx3, sc[c + 6], sc[c + 7]);
         }
         const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
-        const float m_new = fmaxf(m_run, m_tile);
         float alpha = 1.f;
         bool rescale = false;
-        if (m_new > m_run) {
+        if (m_tile > m_run) {
+          // exact rescale by alpha = exp(m_old - m_new) whenever the running max grows
           if (m_run == -INFINITY) {
             alpha = 0.f;            // nothing accumulated yet: the state is zero
           } else {
-            alpha = ex2(m_run - m_new);
+            alpha = ex2(m_run - m_tile);
             rescale = true;
           }
+          m_run = m_tile;
         }
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        m_run = m_new;
-        float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        const float2 cc = make_float2(c2, c2);
+        const float2 mneg = make_float2(-m_use, -m_use);
+        float2 za = make_float2(0.f, 0.f), zb = za, zc = za, zd = za;
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          sc[c] = ex2(fmaf(sc[c], c2, -m_use));
-          sc[c + 1] = ex2(fmaf(sc[c + 1], c2, -m_use));
-          sc[c + 2] = ex2(fmaf(sc[c + 2], c2, -m_use));
-          sc[c + 3] = ex2(fmaf(sc[c + 3], c2, -m_use));
-          z0 += sc[c];
-          z1 += sc[c + 1];
-          z2 += sc[c + 2];
-          z3 += sc[c + 3];
+        for (int c = 0; c < 128; c += 8) {
+          float2 x0 = ffma2(make_float2(sc[c], sc[c + 1]), cc, mneg);
+          float2 x1 = ffma2(make_float2(sc[c + 2], sc[c + 3]), cc, mneg);
+          float2 x2 = ffma2(make_float2(sc[c + 4], sc[c + 5]), cc, mneg);
+          float2 x3 = ffma2(make_float2(sc[c + 6], sc[c + 7]), cc, mneg);
+          x0 = make_float2(ex2(x0.x), ex2(x0.y));
+          x1 = make_float2(ex2(x1.x), ex2(x1.y));
+          x2 = make_float2(ex2(x2.x), ex2(x2.y));
+          x3 = make_float2(ex2(x3.x), ex2(x3.y));
+          za = fadd2(za, x0);
+          zb = fadd2(zb, x1);
+          zc = fadd2(zc, x2);
+          zd = fadd2(zd, x3);
+          sc[c] = x0.x; sc[c + 1] = x0.y; sc[c + 2] = x1.x; sc[c + 3] = x1.y;
+          sc[c + 4] = x2.x; sc[c + 5] = x2.y; sc[c + 6] = x3.x; sc[c + 7] = x3.y;
         }
-        z_run = z_run * alpha + ((z0 + z1) + (z2 + z3));
+        const float2 zs = fadd2(fadd2(za, zb), fadd2(zc, zd));
+        z_run = z_run * alpha + (zs.x + zs.y);
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t pk[32];
@@ -462,14 +495,33 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
         // Rescale this row's O by alpha before P V of this tile is issued (the
         // MMA that produced O so far has completed: see the commit order above).
         if (__any_sync(0xffffffffu, rescale)) {
-          const float a = rescale ? alpha : 1.f;
+          const float2 a2 = rescale ? make_float2(alpha, alpha) : make_float2(1.f, 1.f);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_x32(tO + c * 32, r);
+          for (int c = 0; c < D / 128 + (D % 128 ? 1 : 0); ++c) {
+            if (D >= 128) {
+              uint32_t r[128];
+              tmem_ld_x128(tO + c * 128, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * a);
-            tmem_st_x32(tO + c * 32, r);
+              for (int j = 0; j < 128; j += 2) {
+                const float2 v = fmul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2);
+                r[j] = __float_as_uint(v.x);
+                r[j + 1] = __float_as_uint(v.y);
+              }
+              tmem_st_x128(tO + c * 128, r);
+            } else {
+#pragma unroll
+              for (int c2i = 0; c2i < D / 32; ++c2i) {
+                uint32_t r[32];
+                tmem_ld_x32(tO + c2i * 32, r);
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                  const float2 v = fmul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2);
+                  r[j] = __float_as_uint(v.x);
+                  r[j + 1] = __float_as_uint(v.y);
+                }
+                tmem_st_x32(tO + c2i * 32, r);
+              }
+            }
           }
         }
         tmem_st_wait();
