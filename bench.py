@@ -9,6 +9,8 @@ with inputs resident in HBM. Also measured in the same run:
     copy of Q, K, V and the device->host copy of O, LSE inside the timed region;
   * merge: ring_attn_merge over n=8 per-shard partials of a B=1, N=32768, H=32,
     d=128 problem (HBM-bound), as GB/s against the measured copy bandwidth;
+  * decode: ring_attn_decode of one query token per sequence against the same
+    KV cache (per-shard partials + merge; HBM-bound), as GB/s;
   * cpu_baseline: the fp64 CPU oracle on a bounded sample of query rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--impl ours|reference]
@@ -359,6 +361,36 @@ def run_ours(args, w):
                  "workload": "n=8 parts, B=1, N=32768, H=32, d=128 fp32 partials -> bf16"}
         del o_p, l_p, mo, ml
 
+    # ---- pass-Q decode (HBM-bound): one query token per sequence on the same KV cache
+    decode = None
+    if not args.no_decode:
+        gq = torch.Generator(device=dev)
+        gq.manual_seed(5)
+        qd = torch.randn((w.batch, 1, w.heads, w.head_dim), generator=gq, device=dev,
+                         dtype=torch.float32).to(torch.bfloat16)
+        need = ra.decode_workspace_bytes(w.batch, w.seqlen, w.heads, w.kv_heads, w.head_dim, w.P,
+                                         1, w.layout, w.causal)
+        ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=dev)
+        od = torch.empty((w.batch, 1, w.heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        ld = torch.empty((w.batch, w.heads, 1), dtype=torch.float32, device=dev)
+
+        def dec():
+            ra.decode(qd, k, v, w.P, w.seqlen - 1, w.layout, w.causal, workspace=ws, out=od, lse=ld)
+
+        for _ in range(3):
+            dec()
+        ms = time_launches(dec, max(10, args.steps), stream)
+        dbytes = (k.numel() + v.numel()) * 2 + qd.numel() * 2 + od.numel() * 2 + ld.numel() * 4
+        gbs = dbytes / (statistics.mean(ms) * 1e-3) / 1e9
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        decode = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                  "algorithmic_bytes": dbytes, "ms": statistics.mean(ms),
+                  "launches_per_call": 2,
+                  "workload": f"1 query token per sequence at position N-1 against the {w.name} "
+                              f"KV cache (B={w.batch}, N={w.seqlen}, G={w.kv_heads}, d={w.head_dim}, "
+                              f"P={w.P} {w.layout}); partials per (shard, 2048-key chunk) + merge"}
+        del qd, ws, od, ld
+
     # ---- the oracle on the host cores (rank 0 only)
     cpu = None
     if info.is_main and not args.no_cpu_baseline:
@@ -381,6 +413,7 @@ def run_ours(args, w):
                          "peak_source": f"{peaks_src} bf16 burst",
                          "kernel": "ring_tc_kernel<128>", "launch_ms": statistics.mean(launch_ms)},
             "merge_roofline": merge,
+            "decode_roofline": decode,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -404,6 +437,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-merge", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

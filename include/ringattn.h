@@ -49,6 +49,7 @@
 #ifndef RINGATTN_H
 #define RINGATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -140,6 +141,28 @@ ra_status ring_attn_finalize(const ra_problem* p, const float* m, const float* z
 ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_t heads,
                           int32_t head_dim, const float* o_parts, const float* lse_parts,
                           void* o, float* lse, void* stream);
+
+/* Pass-Q decode: n_q query rows per (batch, head), at global positions
+ * q_pos0 .. q_pos0 + n_q - 1, attend to a KV cache of N tokens that stays sharded
+ * and stationary in P virtual shards (layout as in p). Phase 1: every virtual
+ * device u scores all queries against its own shard only and writes a
+ * normalised partial (O_u, LSE_u) into the workspace (a shard is cut into key
+ * chunks, each one more partial). Phase 2: the partials are combined by the
+ * ring_attn_merge kernel. Under the causal mask a query sees key positions
+ * <= its own. Source: Transformer Math "Ring Attention" (aicassindra), "The ring
+ * is a prefill algorithm" (broadcast the query, partial per shard, one
+ * reduction); "Part 4: Ring Attention" (Fofadiya) §4.9.4.4 (pass-Q).
+ * q [B, n_q, H, d] bf16, k, v [B, N, G, d] bf16 in; o [B, n_q, H, d] bf16 and
+ * lse [B, H, n_q] fp32 out. workspace: caller-owned device memory of at least
+ * ring_attn_decode_workspace_bytes(p, n_q) bytes, 16-byte aligned, overwritten.
+ * 1 <= n_q <= 4096; with causal = 1, q_pos0 + n_q <= N. Two launches on stream. */
+ra_status ring_attn_decode(const ra_problem* p, int32_t n_q, int32_t q_pos0, const void* q,
+                           const void* k, const void* v, void* o, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ring_attn_decode needs for this problem and n_q (0 if the
+ * arguments are invalid). Pure host code. */
+size_t ring_attn_decode_workspace_bytes(const ra_problem* p, int32_t n_q);
 
 /* Shard ownership on the HOST: owner[t], local[t] for t < N and
  * token_of[u*S + i] (S = N/P) for the given layout. Pure host code; host

@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import (LAYOUTS, RA_ERR_CUDA, RA_ERR_INVALID_ARG, RA_ERR_TIMEOUT,  # noqa: F401
                    RA_ERR_UNSUPPORTED, RA_OK, TILE, RingAttnError, check, load)
 
-__all__ = ["fwd", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
+__all__ = ["fwd", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
            "tile_classes", "mask", "last_error", "selftest_timeout", "problem", "RingAttnError",
            "empty_state", "LAYOUTS", "TILE"]
 
@@ -83,6 +83,47 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str =
     with torch.cuda.device(q.device):
         check("ring_attn_fwd", lib.ring_attn_fwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v),
                                                  _ptr(out), _ptr(lse), _stream(q.device)))
+    return out, lse
+
+
+def decode_workspace_bytes(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int,
+                           P: int, n_q: int, layout: str = "contiguous", causal: bool = True) -> int:
+    """Workspace bytes ring_attn_decode needs (ring_attn_decode_workspace_bytes)."""
+    lib = load()
+    pr = problem(batch, seqlen, heads, kv_heads, head_dim, P, causal, layout)
+    return int(lib.ring_attn_decode_workspace_bytes(ctypes.byref(pr), int(n_q)))
+
+
+def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, q_pos0: int,
+           layout: str = "contiguous", causal: bool = True, scale: float = 0.0,
+           workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None):
+    """Pass-Q decode (ring_attn_decode): q [B, n_q, H, d] at positions q_pos0.. against the
+    KV cache k, v [B, N, G, d] in P stationary virtual shards. Returns (O, LSE)."""
+    lib = load()
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, n_q, H, d] and k, v [B, N, G, d]")
+    B, n_q, H, d = q.shape
+    N, G = k.shape[1], k.shape[2]
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16, (B, N, G, d))
+    _need(v, "v", torch.bfloat16, (B, N, G, d))
+    pr = problem(B, N, H, G, d, P, causal, layout, scale)
+    need = int(lib.ring_attn_decode_workspace_bytes(ctypes.byref(pr), n_q))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16) // 4 + 4, dtype=torch.float32, device=q.device)
+    _need(workspace, "workspace", torch.float32)
+    if out is None:
+        out = torch.empty((B, n_q, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, n_q, H, d))
+    _need(lse, "lse", torch.float32, (B, H, n_q))
+    with torch.cuda.device(q.device):
+        check("ring_attn_decode", lib.ring_attn_decode(
+            ctypes.byref(pr), int(n_q), int(q_pos0), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+            _ptr(lse), _ptr(workspace), ctypes.c_size_t(workspace.numel() * 4),
+            _stream(q.device)))
     return out, lse
 
 

@@ -185,6 +185,19 @@ ra_status check_step_args(const ra_problem* pr, int32_t s, const void* q, const 
   return RA_OK;
 }
 
+// Number of partials the decode phase writes (one per shard and key chunk).
+int64_t decode_parts(const ra_problem* pr) {
+  const int S = pr->seqlen / pr->P;
+  const int chunk = decode_chunk_keys(S);
+  return static_cast<int64_t>(pr->P) * ((S + chunk - 1) / chunk);
+}
+
+size_t decode_workspace(const ra_problem* pr, int32_t n_q) {
+  const size_t parts = static_cast<size_t>(decode_parts(pr));
+  const size_t rows = static_cast<size_t>(pr->batch) * pr->heads * n_q;
+  return parts * rows * (static_cast<size_t>(pr->head_dim) + 1) * sizeof(float);
+}
+
 }  // namespace
 
 extern "C" {
@@ -347,6 +360,47 @@ ra_status ring_attn_mask(const ra_problem* pr, int32_t u, int32_t b, uint8_t* ma
   RingParams p;
   fill_params(pr, &p);
   return launch_result(launch_mask(p, u, b, mask, static_cast<cudaStream_t>(stream)));
+}
+
+size_t ring_attn_decode_workspace_bytes(const ra_problem* pr, int32_t n_q) {
+  if (check_problem(pr) != RA_OK || n_q < 1) return 0;
+  return decode_workspace(pr, n_q);
+}
+
+ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, const void* q,
+                           const void* k, const void* v, void* o, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  if (n_q < 1 || n_q > 4096 || q_pos0 < 0) return RA_ERR_INVALID_ARG;
+  if (pr->causal && static_cast<int64_t>(q_pos0) + n_q > pr->seqlen) return RA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse || !workspace) return RA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return RA_ERR_INVALID_ARG;
+  if (workspace_bytes < decode_workspace(pr, n_q)) return RA_ERR_INVALID_ARG;
+  const int64_t parts = decode_parts(pr);
+  const int64_t rows_total = static_cast<int64_t>(pr->heads / pr->kv_heads) * n_q;
+  const int64_t rowgroups = (rows_total + 31) / 32;
+  if (parts > 1024 || pr->P > 65535 ||
+      static_cast<int64_t>(pr->batch) * pr->kv_heads * rowgroups > 65535 || pr->batch > 65535 ||
+      pr->heads > 65535)
+    return RA_ERR_UNSUPPORTED;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams p;
+  fill_params(pr, &p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.status = d->status;
+  float* o_parts = static_cast<float*>(workspace);
+  float* lse_parts = o_parts + static_cast<size_t>(parts) * pr->batch * n_q * pr->heads * pr->head_dim;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_partials(p, n_q, q_pos0, o_parts, lse_parts, cs);
+  if (e != cudaSuccess) return RA_ERR_CUDA;
+  return launch_result(launch_merge(static_cast<int>(parts), pr->batch, n_q, pr->heads,
+                                    pr->head_dim, o_parts, lse_parts, o, lse, cs));
 }
 
 ra_status ring_attn_last_error(int32_t* device_code) {

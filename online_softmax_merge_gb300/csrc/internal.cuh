@@ -51,6 +51,11 @@ cudaError_t launch_tile_classes(const RingParams& p, int u, int b, int8_t* class
                                 cudaStream_t st);
 cudaError_t launch_mask(const RingParams& p, int u, int b, uint8_t* mask, cudaStream_t st);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t st);
+// Pass-Q decode, phase 1: per-(shard, key chunk) partials into the workspace.
+cudaError_t launch_decode_partials(const RingParams& p, int n_q, int q_pos0, float* o_parts,
+                                   float* lse_parts, cudaStream_t st);
+// Keys per chunk of a shard in the decode partial phase.
+int decode_chunk_keys(int S);
 
 // Bytes of dynamic shared memory the tensor-core kernel uses for head_dim D.
 int ring_tc_smem_bytes(int D);

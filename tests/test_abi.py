@@ -23,7 +23,7 @@ def lib():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|ra_status|int32_t)\s+(\w+)\s*\(",
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|ra_status|int32_t|size_t)\s+(\w+)\s*\(",
                                  text, flags=re.M)))
 
 
@@ -103,3 +103,17 @@ def test_host_shard_map_rejects_bad_sizes(lib):
     assert lib.ring_attn_shard_map(0, 10, 3, arr, arr, arr) == _lib.RA_ERR_INVALID_ARG
     assert lib.ring_attn_shard_map(5, 10, 2, arr, arr, arr) == _lib.RA_ERR_INVALID_ARG
     assert lib.ring_attn_shard_map(0, 10, 2, None, arr, arr) == _lib.RA_ERR_INVALID_ARG
+
+
+def test_decode_workspace_and_argument_checks(lib):
+    pr = _pr(seqlen=8192, P=4)                       # S = 2048: one chunk per shard
+    need = lib.ring_attn_decode_workspace_bytes(ctypes.byref(pr), 3)
+    assert need == 4 * 1 * 4 * 3 * (128 + 1) * 4     # parts * B * H * n_q * (d + 1) floats
+    assert lib.ring_attn_decode_workspace_bytes(ctypes.byref(_pr(heads=3)), 3) == 0
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]
+    assert lib.ring_attn_decode(ctypes.byref(pr), 3, 8189, *args, need - 4, None) == \
+        _lib.RA_ERR_INVALID_ARG                      # workspace too small
+    assert lib.ring_attn_decode(ctypes.byref(pr), 3, 8190, *args, need, None) == \
+        _lib.RA_ERR_INVALID_ARG                      # query positions past the cache
+    assert lib.ring_attn_decode(ctypes.byref(pr), 0, 0, *args, need, None) == \
+        _lib.RA_ERR_INVALID_ARG
