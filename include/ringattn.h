@@ -164,6 +164,27 @@ ra_status ring_attn_decode(const ra_problem* p, int32_t n_q, int32_t q_pos0, con
  * arguments are invalid). Pure host code. */
 size_t ring_attn_decode_workspace_bytes(const ra_problem* p, int32_t n_q);
 
+/* Size of the fixed device scratch ring_attn_decode_noalloc keeps its partials in. */
+#define RA_DECODE_SCRATCH_BYTES (16u << 20)
+
+/* Decode for callers that cannot allocate device memory when they decode (a
+ * serving loop that must not stall on an allocator, a plugin whose host owns all
+ * device memory, a runtime that plans memory up front). Same contract and result
+ * as ring_attn_decode, but the partials go to a fixed scratch array of
+ * RA_DECODE_SCRATCH_BYTES bytes in the library's static device memory (reserved
+ * on every GPU that loads the library, until the process exits) instead of a
+ * caller workspace; the call allocates nothing. There is no counterpart in the
+ * pages: this is an interface choice of this library.
+ * Returns RA_ERR_INVALID_ARG when ring_attn_decode_workspace_bytes(p, n_q) exceeds
+ * RA_DECODE_SCRATCH_BYTES. The first call on a device looks up the scratch
+ * address (cudaGetSymbolAddress) with that device current; make that first call
+ * before capturing a stream. All calls on a device share the scratch and each
+ * call overwrites it: calls whose work may overlap on the GPU (different streams
+ * without ordering) race. */
+ra_status ring_attn_decode_noalloc(const ra_problem* p, int32_t n_q, int32_t q_pos0,
+                                   const void* q, const void* k, const void* v, void* o,
+                                   float* lse, void* stream);
+
 /* Shard ownership on the HOST: owner[t], local[t] for t < N and
  * token_of[u*S + i] (S = N/P) for the given layout. Pure host code; host
  * pointers, each N int32. Source: as for ra_layout. */
