@@ -388,7 +388,7 @@ def run_ours(args, w):
                   "launches_per_call": 2,
                   "workload": f"1 query token per sequence at position N-1 against the {w.name} "
                               f"KV cache (B={w.batch}, N={w.seqlen}, G={w.kv_heads}, d={w.head_dim}, "
-                              f"P={w.P} {w.layout}); partials per (shard, 2048-key chunk) + merge"}
+                              f"P={w.P} {w.layout}); partials per (shard, 4096-key chunk) + merge"}
         del qd, ws, od, ld
 
     # ---- the oracle on the host cores (rank 0 only)

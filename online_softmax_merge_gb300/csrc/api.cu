@@ -380,10 +380,8 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
     return RA_ERR_INVALID_ARG;
   if (workspace_bytes < decode_workspace(pr, n_q)) return RA_ERR_INVALID_ARG;
   const int64_t parts = decode_parts(pr);
-  const int64_t rows_total = static_cast<int64_t>(pr->heads / pr->kv_heads) * n_q;
-  const int64_t rowgroups = (rows_total + 31) / 32;
-  if (parts > 1024 || pr->P > 65535 ||
-      static_cast<int64_t>(pr->batch) * pr->kv_heads * rowgroups > 65535 || pr->batch > 65535 ||
+  // launch limits of the partial phase (grid z = batch * P) and of the merge
+  if (parts > 1024 || static_cast<int64_t>(pr->batch) * pr->P > 65535 || pr->batch > 65535 ||
       pr->heads > 65535)
     return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;

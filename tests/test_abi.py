@@ -106,7 +106,7 @@ def test_host_shard_map_rejects_bad_sizes(lib):
 
 
 def test_decode_workspace_and_argument_checks(lib):
-    pr = _pr(seqlen=8192, P=4)                       # S = 2048: one chunk per shard
+    pr = _pr(seqlen=8192, P=4)                       # S = 2048: one key chunk per shard
     need = lib.ring_attn_decode_workspace_bytes(ctypes.byref(pr), 3)
     assert need == 4 * 1 * 4 * 3 * (128 + 1) * 4     # parts * B * H * n_q * (d + 1) floats
     assert lib.ring_attn_decode_workspace_bytes(ctypes.byref(_pr(heads=3)), 3) == 0
