@@ -12,6 +12,11 @@ The ring cuts the token axis into P shards of S = N / P tokens:
     alternates shard ownership).  N must be divisible by P ("...near-infinite
     context paper...", "Production tradeoffs": devices must divide the
     sequence length evenly).
+  * zigzag: the sequence is cut into 2P chunks of C = N / 2P tokens and shard u
+    holds chunk u (local 0 .. C-1) then chunk 2P-1-u (local C .. 2C-1)
+    ("Part 4: Ring Attention" 4.8.3 "Zigzag (Striped) Load Balancing"; Transformer
+    Math "Ring Attention" (aicassindra), "Causal masking wastes half the ring").
+    N must be divisible by 2P.
 The causal mask is defined on global positions: key position <= query position
 ("...near-infinite context paper...", "The causal masking complication";
 Transformer Math "Ring Attention" (aicassindra), "Composing with tensor
@@ -24,6 +29,8 @@ from typing import List, Tuple
 
 CONTIGUOUS = "contiguous"
 STRIPED = "striped"
+ZIGZAG = "zigzag"
+LAYOUTS = (CONTIGUOUS, STRIPED, ZIGZAG)
 
 TILE_EMPTY = 0      # no admitted pair: skipped
 TILE_PARTIAL = 1    # some pairs admitted: needs an element mask
@@ -31,28 +38,40 @@ TILE_FULL = 2       # every pair admitted: no mask
 
 
 def _check(layout: str, N: int, P: int) -> int:
-    if layout not in (CONTIGUOUS, STRIPED):
+    if layout not in LAYOUTS:
         raise ValueError(f"unknown layout {layout!r}")
     if N <= 0 or P <= 0 or N % P != 0:
         raise ValueError("N and P must be positive with N divisible by P")
+    if layout == ZIGZAG and N % (2 * P) != 0:
+        raise ValueError("zigzag needs N divisible by 2P")
     return N // P
 
 
 def owner(layout: str, N: int, P: int, t: int) -> int:
     """Shard that holds global token t."""
     S = _check(layout, N, P)
+    if layout == ZIGZAG:
+        c = t // (S // 2)                  # chunk of the token
+        return c if c < P else 2 * P - 1 - c
     return t // S if layout == CONTIGUOUS else t % P
 
 
 def local_index(layout: str, N: int, P: int, t: int) -> int:
     """Position of token t inside its shard."""
     S = _check(layout, N, P)
+    if layout == ZIGZAG:
+        C = S // 2
+        c = t // C
+        return t % C if c < P else C + t % C
     return t % S if layout == CONTIGUOUS else t // P
 
 
 def token_of(layout: str, N: int, P: int, u: int, i: int) -> int:
     """Global token (= global position) of local index i in shard u."""
     S = _check(layout, N, P)
+    if layout == ZIGZAG:
+        C = S // 2
+        return u * C + i if i < C else (2 * P - 1 - u) * C + (i - C)
     return u * S + i if layout == CONTIGUOUS else i * P + u
 
 

@@ -45,7 +45,7 @@ def test_bad_sizes_rejected():
     with pytest.raises(ValueError):
         OS.shard_map("contiguous", 10, 3)
     with pytest.raises(ValueError):
-        OS.shard_map("zigzag", 8, 2)
+        OS.shard_map("spiral", 8, 2)
 
 
 def test_causal_block_count_matches_printed():
@@ -123,3 +123,70 @@ def test_ring_visit_order_matches_printed_schedule():
             assert OR.ring_order(int(u), P)[step] == b
     for u in range(P):
         assert sorted(OR.ring_order(u, P)) == list(range(P))
+
+
+# --------------------------------------------------------------------------- zigzag
+
+def test_zigzag_map_by_hand():
+    # N = 8, P = 2: chunks of 2 tokens; shard 0 = chunks 0 and 3, shard 1 = chunks 1 and 2
+    own, loc, tok = OS.shard_map("zigzag", 8, 2)
+    assert tok == [0, 1, 6, 7, 2, 3, 4, 5]
+    assert own == [0, 0, 1, 1, 1, 1, 0, 0]
+    assert loc == [0, 1, 0, 1, 2, 3, 2, 3]
+
+
+@pytest.mark.parametrize("N,P", [(16, 4), (48, 3), (256, 8), (10, 5)])
+def test_zigzag_maps_are_inverse_bijections(N, P):
+    own, loc, tok = OS.shard_map("zigzag", N, P)
+    S = N // P
+    assert sorted(tok) == list(range(N))
+    for t in range(N):
+        assert tok[own[t] * S + loc[t]] == t
+
+
+def test_zigzag_needs_2p_chunks():
+    with pytest.raises(ValueError):
+        OS.shard_map("zigzag", 12, 4)       # 12 % 8 != 0
+
+
+def test_zigzag_assignment_matches_printed():
+    g = json.load(open(os.path.join(GOLDEN, "zigzag.json")))
+    P = g["devices"]
+    C = 3
+    N = 2 * P * C
+    for u, blocks in g["blocks_of_device"].items():
+        toks = OS.shard_tokens("zigzag", N, P, int(u))
+        assert sorted({t // C for t in toks}) == sorted(blocks)
+        assert [t // C for t in toks] == [blocks[0]] * C + [blocks[1]] * C
+
+
+def test_zigzag_balances_causal_block_work_as_printed():
+    g = json.load(open(os.path.join(GOLDEN, "zigzag.json")))
+    P = g["devices"]
+    C = 2
+    N = 2 * P * C
+    # units: (query chunk of the device, key chunk) pairs with any visible element
+    for u in range(P):
+        toks = OS.shard_tokens("zigzag", N, P, u)
+        qchunks = sorted({t // C for t in toks})
+        units = sum(1 for qc in qchunks for kc in range(2 * P)
+                    if any(kc * C + j <= qc * C + i for i in range(C) for j in range(C)))
+        assert units == g["small_block_units_per_device"]
+    # the printed speedups: contiguous bottleneck P big blocks vs (2P+1)/4 equivalents
+    for n, want in g["speedup"].items():
+        n = int(n)
+        assert round(n / ((2 * n + 1) / 4), 2) == want
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_equals_dense_zigzag(causal):
+    import numpy as np
+    from oracle import attention as OA
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((1, 48, 4, 8))
+    k = rng.standard_normal((1, 48, 2, 8))
+    v = rng.standard_normal((1, 48, 2, 8))
+    O, L = OA.dense_attention(q, k, v, causal=causal)
+    for P in (1, 2, 3, 4, 6):
+        Or_, Lr = OR.ring_attention(q, k, v, P, "zigzag", causal)
+        assert np.abs(Or_ - O).max() < 1e-12 and np.abs(Lr - L).max() < 1e-12
