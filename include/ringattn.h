@@ -65,10 +65,14 @@ typedef enum {
 } ra_status;
 
 /* Shard layouts ("Part 4: Ring Attention" §4.3.1 for contiguous; "Ring Attention"
- * (aarnphm.xyz): striped ownership alternates, token t -> shard t mod P). */
+ * (aarnphm.xyz): striped ownership alternates, token t -> shard t mod P; "Part 4"
+ * §4.8.3 and Transformer Math "Ring Attention" (aicassindra), "Causal masking
+ * wastes half the ring", for zigzag). */
 typedef enum {
   RA_LAYOUT_CONTIGUOUS = 0, /* shard u = tokens [u*S, (u+1)*S), local i -> token u*S + i */
-  RA_LAYOUT_STRIPED = 1     /* token t -> shard t mod P, local index t div P */
+  RA_LAYOUT_STRIPED = 1,    /* token t -> shard t mod P, local index t div P */
+  RA_LAYOUT_ZIGZAG = 2      /* 2P chunks of C = N/(2P): shard u = chunk u (local 0..C-1)
+                               then chunk 2P-1-u (local C..2C-1); needs N % (2P) == 0 */
 } ra_layout;
 
 /* Tile classes of a (query tile, key tile) pair ("Part 4" §4.8.1 "Skipping
@@ -81,7 +85,7 @@ typedef enum { RA_TILE_EMPTY = 0, RA_TILE_PARTIAL = 1, RA_TILE_FULL = 2 } ra_til
 
 typedef struct {
   int32_t batch;      /* B >= 1 */
-  int32_t seqlen;     /* N >= 1, N % P == 0, N < 2^30 */
+  int32_t seqlen;     /* N >= 1, N % P == 0 (zigzag: N % 2P == 0), N < 2^30 */
   int32_t heads;      /* H >= 1 */
   int32_t kv_heads;   /* G >= 1, H % G == 0 */
   int32_t head_dim;   /* d in {64, 128} */

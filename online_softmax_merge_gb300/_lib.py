@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(HERE, "libringattn.so")
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
 STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
                 4: "RA_ERR_TIMEOUT"}
-LAYOUTS = {"contiguous": 0, "striped": 1}
+LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
 TILE = 128
 
 # Every exported function of include/ringattn.h, with (restype, argtypes).

@@ -53,6 +53,15 @@ ra_status current_device(DevInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+ra_status check_layout_sizes(int32_t layout, int32_t seqlen, int32_t P) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED && layout != RA_LAYOUT_ZIGZAG)
+    return RA_ERR_INVALID_ARG;
+  if (seqlen < 1 || P < 1 || P > seqlen || seqlen % P != 0 || seqlen >= (1 << 30))
+    return RA_ERR_INVALID_ARG;
+  if (layout == RA_LAYOUT_ZIGZAG && seqlen % (2 * P) != 0) return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
 ra_status check_problem(const ra_problem* pr) {
   if (pr == nullptr) return RA_ERR_INVALID_ARG;
   if (pr->batch < 1 || pr->seqlen < 1 || pr->heads < 1 || pr->kv_heads < 1 || pr->P < 1)
@@ -61,8 +70,10 @@ ra_status check_problem(const ra_problem* pr) {
     return RA_ERR_INVALID_ARG;
   if (pr->heads % pr->kv_heads != 0) return RA_ERR_INVALID_ARG;
   if (pr->causal != 0 && pr->causal != 1) return RA_ERR_INVALID_ARG;
-  if (pr->layout != RA_LAYOUT_CONTIGUOUS && pr->layout != RA_LAYOUT_STRIPED)
+  if (pr->layout != RA_LAYOUT_CONTIGUOUS && pr->layout != RA_LAYOUT_STRIPED &&
+      pr->layout != RA_LAYOUT_ZIGZAG)
     return RA_ERR_INVALID_ARG;
+  if (pr->layout == RA_LAYOUT_ZIGZAG && pr->seqlen % (2 * pr->P) != 0) return RA_ERR_INVALID_ARG;
   if (!(pr->scale >= 0.f) || isinf(pr->scale)) return RA_ERR_INVALID_ARG;
   if (pr->head_dim != 64 && pr->head_dim != 128) return RA_ERR_UNSUPPORTED;
   // every tensor's element count must fit the kernels' 64-bit offsets and the
@@ -85,7 +96,9 @@ void fill_params(const ra_problem* pr, RingParams* p) {
   p->causal = pr->causal;
   const int hpg = p->H / p->G;
   p->pair_heads = (hpg % 2 == 0) ? 1 : 0;
-  p->nq = (p->S + 127) / 128;
+  p->X = p->layout == kZigzag ? 2 * p->P : p->P;
+  p->L = p->layout == kZigzag ? p->S / 2 : p->S;
+  p->nq = (p->L + 127) / 128;
   if (p->pair_heads) {
     p->pairs_per_g = hpg / 2;
     p->nqq = p->nq;
@@ -93,7 +106,7 @@ void fill_params(const ra_problem* pr, RingParams* p) {
     p->pairs_per_g = hpg;
     p->nqq = (p->nq + 1) / 2;
   }
-  p->units_per_bg = p->pairs_per_g * p->P * p->nqq;
+  p->units_per_bg = p->pairs_per_g * p->X * p->nqq;
   const double sc = pr->scale > 0.f ? static_cast<double>(pr->scale) : 1.0 / sqrt(static_cast<double>(p->D));
   p->scale = static_cast<float>(sc);
   p->scale_log2 = static_cast<float>(sc * 1.4426950408889634);
@@ -165,10 +178,12 @@ bool encode_rows(CUtensorMap* m, const void* base, int B, int N, int heads, int 
 ra_status launch_result(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
 
 ra_status run_tc(const RingParams& p, cudaStream_t st) {
+  // zigzag tiles by chunk: the contiguous view with X = 2P chunks of L = S/2 tokens
+  const int ml = p.layout == kZigzag ? kContiguous : p.layout;
   CUtensorMap tq, tk, tv;
-  if (!encode_rows(&tq, p.q, p.B, p.N, p.H, p.D, p.S, p.P, p.layout) ||
-      !encode_rows(&tk, p.k, p.B, p.N, p.G, p.D, p.S, p.P, p.layout) ||
-      !encode_rows(&tv, p.v, p.B, p.N, p.G, p.D, p.S, p.P, p.layout))
+  if (!encode_rows(&tq, p.q, p.B, p.N, p.H, p.D, p.L, p.X, ml) ||
+      !encode_rows(&tk, p.k, p.B, p.N, p.G, p.D, p.L, p.X, ml) ||
+      !encode_rows(&tv, p.v, p.B, p.N, p.G, p.D, p.L, p.X, ml))
     return RA_ERR_CUDA;
   return launch_result(launch_ring_tc(p, tq, tk, tv, st));
 }
@@ -312,9 +327,7 @@ ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_
 
 ra_status ring_attn_shard_map(int32_t layout, int32_t seqlen, int32_t P, int32_t* owner,
                               int32_t* local, int32_t* token_of) {
-  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED) return RA_ERR_INVALID_ARG;
-  if (seqlen < 1 || P < 1 || P > seqlen || seqlen % P != 0 || seqlen >= (1 << 30))
-    return RA_ERR_INVALID_ARG;
+  if (check_layout_sizes(layout, seqlen, P) != RA_OK) return RA_ERR_INVALID_ARG;
   if (!owner || !local || !token_of) return RA_ERR_INVALID_ARG;
   const int32_t S = seqlen / P;
   for (int32_t t = 0; t < seqlen; ++t) {
@@ -327,9 +340,7 @@ ra_status ring_attn_shard_map(int32_t layout, int32_t seqlen, int32_t P, int32_t
 
 ra_status ring_attn_shard_map_device(int32_t layout, int32_t seqlen, int32_t P, int32_t* owner,
                                      int32_t* local, int32_t* token_of, void* stream) {
-  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED) return RA_ERR_INVALID_ARG;
-  if (seqlen < 1 || P < 1 || P > seqlen || seqlen % P != 0 || seqlen >= (1 << 30))
-    return RA_ERR_INVALID_ARG;
+  if (check_layout_sizes(layout, seqlen, P) != RA_OK) return RA_ERR_INVALID_ARG;
   if (!owner || !local || !token_of) return RA_ERR_INVALID_ARG;
   DevInfo* d = nullptr;
   ra_status st = current_device(&d);

@@ -141,10 +141,12 @@ decode_partial_kernel(const RingParams p, int n_q, int q_pos0, int chunk, int n_
 #pragma unroll
   for (int r = 0; r < RB; ++r)
     if (r < n_rows) qpos_max = max(qpos_max, q_pos0 + (row0 + r) % n_q);
-  const int n_vis = j_end > j_begin
-                        ? visible_prefix(p.layout, p.S, p.P, p.causal, u, j_begin,
-                                         j_end - j_begin, qpos_max)
-                        : 0;
+  // keys of the chunk some row may see: a prefix of the chunk, except for zigzag
+  // shards whose chunk may span both halves (then the per-key rule alone decides)
+  const int n_vis = j_end <= j_begin ? 0
+                    : p.layout == kZigzag ? j_end - j_begin
+                                          : visible_prefix(p.layout, p.S, p.P, p.causal, u, j_begin,
+                                                           j_end - j_begin, qpos_max);
   const int j_stop = j_begin + n_vis;
 
   // This lane's query columns of every row, pre-scaled by scale * log2(e), with
@@ -234,7 +236,7 @@ decode_partial_kernel(const RingParams p, int n_q, int q_pos0, int chunk, int n_
     // lane owns pair (my_k, my_r): its score, masked when invisible
     const int jj = j0 + my_k;
     const bool vis = jj < j_stop && my_r < n_rows &&
-                     visible_prefix(p.layout, p.S, p.P, p.causal, u, jj, 1, my_qpos) > 0;
+                     key_visible(p.layout, p.S, p.P, p.causal, u, jj, my_qpos);
     const float s_own = vis ? dots[0] : -INFINITY;
     // online softmax of each row over the group's keys (lanes of one row differ by RB)
     float mx = s_own;

@@ -16,8 +16,10 @@ struct RingParams {
   // sub-tiles. pair_heads = 1: two query heads of one kv group, same rows;
   // pair_heads = 0: one head, two consecutive 128-row tiles.
   int32_t pair_heads;
-  int32_t nq;             // 128-row query tiles per shard, ceil(S / 128)
-  int32_t nqq;            // query units per shard and head pair
+  int32_t X, L;           // query rows are tiled per chunk: X chunks of L rows
+                          // (contiguous, striped: X = P, L = S; zigzag: X = 2P, L = S/2)
+  int32_t nq;             // 128-row query tiles per chunk, ceil(L / 128)
+  int32_t nqq;            // query units per chunk and head pair
   int32_t pairs_per_g;    // head pairs (or heads) per kv head
   int32_t units_per_bg;   // CTAs per (batch, kv head)
   // Which ring steps this launch folds: s in [s_begin, s_end).

@@ -3,7 +3,7 @@
 //  * shard ownership: owner[t], local[t], token_of[u*S + i] for a layout;
 //  * tile classes of a (u, b) shard pair ("Part 4: Ring Attention" (Fofadiya)
 //    §4.8.1 "Skipping Fully-Masked Blocks");
-//  * the element mask of a (u, b) shard pair from the per-row visible prefix.
+//  * the element mask of a (u, b) shard pair from the kernels' per-key visibility.
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "shardmap.cuh"
@@ -40,8 +40,7 @@ __global__ void mask_kernel(int layout, int S, int P, int causal, int u, int b, 
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int i = static_cast<int>(idx / S), j = static_cast<int>(idx % S);
     const int qpos = pos_of(layout, S, P, u, i);
-    const int cnt = visible_prefix(layout, S, P, causal, b, 0, S, qpos);
-    mask[idx] = j < cnt ? 1 : 0;
+    mask[idx] = visible_prefix(layout, S, P, causal, b, j, 1, qpos) > 0 ? 1 : 0;
   }
 }
 

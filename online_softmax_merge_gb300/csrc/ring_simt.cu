@@ -57,7 +57,10 @@ ring_simt_kernel(const RingParams p, int s) {
   for (int c = lane; c < D; c += 32)
     qs[warp][c] = valid ? __bfloat162float(q[yo + c]) : 0.f;
 
-  const int n_vis = valid ? visible_prefix(p.layout, p.S, p.P, p.causal, b, 0, p.S, qpos) : 0;
+  // keys that may be visible: a prefix of the shard except for zigzag (two runs)
+  const int n_vis = !valid ? 0
+                    : p.layout == kZigzag ? p.S
+                                          : visible_prefix(p.layout, p.S, p.P, p.causal, b, 0, p.S, qpos);
   // The block walks the union of its rows' visible prefixes.
   int n_blk = n_vis;
   n_blk = __reduce_max_sync(0xffffffffu, n_blk);
@@ -88,7 +91,8 @@ ring_simt_kernel(const RingParams p, int s) {
     float sdot = 0.f;
 #pragma unroll 8
     for (int c = 0; c < D; ++c) sdot = fmaf(qs[warp][c], ks[jj][c], sdot);
-    float sc = (j0 + jj < n_vis) ? sdot * p.scale : -INFINITY;
+    const bool vis = (j0 + jj < n_vis) && key_visible(p.layout, p.S, p.P, p.causal, b, j0 + jj, qpos);
+    float sc = vis ? sdot * p.scale : -INFINITY;
     float bm = sc;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));

@@ -68,8 +68,9 @@ enum : int {
 
 struct Unit {
   int bat, g, u;
+  int seg;        // segment of shard u the query rows lie in
   int head[2];
-  int row0[2];
+  int row0[2];    // first row of each sub-tile, relative to the segment
   int qpos_max;   // latest global query position held by the CTA, -1 if none
 };
 
@@ -82,15 +83,24 @@ __device__ __forceinline__ Unit decode_unit(const RingParams& p, int idx) {
   const int hp = r % p.pairs_per_g;
   r /= p.pairs_per_g;
   // Within one (batch, kv head), launch the latest query positions first: under
-  // a causal mask they carry the most key tiles.
-  const int key = p.P * p.nqq - 1 - r;
-  int qq;
-  if (p.layout == kContiguous) {
-    w.u = key / p.nqq;
-    qq = key - w.u * p.nqq;
-  } else {
+  // a causal mask they carry the most key tiles. Query tiles are enumerated per
+  // chunk of L rows (a shard, or a zigzag half-shard); positions grow with
+  // (chunk, tile) for contiguous and zigzag, and with (tile, shard) for striped.
+  const int key = p.X * p.nqq - 1 - r;
+  int qq, c;
+  if (p.layout == kStriped) {
     qq = key / p.P;
-    w.u = key - qq * p.P;
+    c = key - qq * p.P;
+  } else {
+    c = key / p.nqq;
+    qq = key - c * p.nqq;
+  }
+  if (p.layout == kZigzag) {
+    w.u = c < p.P ? c : 2 * p.P - 1 - c;
+    w.seg = c < p.P ? 0 : 1;
+  } else {
+    w.u = c;
+    w.seg = 0;
   }
   const int hpg = p.H / p.G;
   if (p.pair_heads) {
@@ -102,12 +112,13 @@ __device__ __forceinline__ Unit decode_unit(const RingParams& p, int idx) {
     w.row0[0] = 2 * qq * 128;
     w.row0[1] = w.row0[0] + 128;
   }
+  const Seg sq = seg_of(p.layout, p.S, p.P, w.u, w.seg);
   w.qpos_max = -1;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    if (w.row0[i] < p.S) {
-      const int last = min(w.row0[i] + 127, p.S - 1);
-      w.qpos_max = max(w.qpos_max, pos_of(p.layout, p.S, p.P, w.u, last));
+    if (w.row0[i] < sq.len) {
+      const int last = min(w.row0[i] + 127, sq.len - 1);
+      w.qpos_max = max(w.qpos_max, sq.base + last * sq.stride);
     }
   }
   return w;
@@ -118,22 +129,23 @@ __device__ __forceinline__ int shard_at(const RingParams& p, int u, int s) {
   return b < 0 ? b + p.P : b;
 }
 
-// Key tiles of shard b that some query of the CTA may see (a prefix of the shard).
-__device__ __forceinline__ int kv_tiles(const RingParams& p, int b, int qpos_max) {
-  const int n = visible_prefix(p.layout, p.S, p.P, p.causal, b, 0, p.S, qpos_max);
+// Key tiles of segment g that some query of the CTA may see (a prefix of it).
+__device__ __forceinline__ int kv_tiles(const RingParams& p, const Seg& g, int qpos_max) {
+  const int n = seg_visible(g, p.causal, 0, g.len, qpos_max);
   return (n + 127) >> 7;
 }
 
-// TMA box coordinates (innermost first) of 128 rows starting at local row i0
-// of shard u: the tensor maps view [B, N, heads, d] as (d, heads, S, P, B) for
-// the contiguous layout and (d, heads, P, S, B) for the striped one.
+// TMA box coordinates (innermost first) of 128 rows starting at row i0 of a
+// segment: the tensor maps view [B, N, heads, d] as (d, heads, L, X, B) for the
+// contiguous and zigzag layouts (X chunks of L tokens; the segment's chunk index)
+// and as (d, heads, P, S, B) for the striped one (the segment's shard).
 __device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, uint32_t bar,
-                                         int layout, int chunk, int head, int u, int i0,
+                                         int layout, int dchunk, int head, int chunk, int i0,
                                          int bat) {
-  if (layout == kContiguous)
-    tma_load_5d(dst, map, bar, chunk * 64, head, i0, u, bat);
+  if (layout == kStriped)
+    tma_load_5d(dst, map, bar, dchunk * 64, head, chunk, i0, bat);
   else
-    tma_load_5d(dst, map, bar, chunk * 64, head, u, i0, bat);
+    tma_load_5d(dst, map, bar, dchunk * 64, head, i0, chunk, bat);
 }
 
 __device__ __forceinline__ void record_failure(const RingParams& p, volatile int* abort_flag) {
@@ -170,7 +182,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
   }
 }
 
-template <int D>
+// ZIG: zigzag layout (two key segments per shard); otherwise one segment.
+template <int D, bool ZIG>
 __global__ void __launch_bounds__(kThreads, 1)
 ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUtensorMap tq,
                const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
@@ -189,7 +202,10 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
 
   // Number of key tiles this CTA folds (every role walks the same sequence).
   int T = 0;
-  for (int s = p.s_begin; s < p.s_end; ++s) T += kv_tiles(p, shard_at(p, w.u, s), w.qpos_max);
+  for (int s = p.s_begin; s < p.s_end; ++s)
+    for (int ks = 0; ks < (ZIG ? 2 : 1); ++ks)
+      T += kv_tiles(p, seg_of(p.layout, p.S, p.P, shard_at(p, w.u, s), ks), w.qpos_max);
+  const Seg sq = seg_of(p.layout, p.S, p.P, w.u, w.seg);   // segment of the query rows
 
   if (T == 0) {
     // Only in step mode: this shard is invisible to every row of the CTA, so the
@@ -197,8 +213,8 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     if (p.step_mode && !p.load_state && threadIdx.x < 256) {
       const int i = threadIdx.x >> 7;
       const int row = w.row0[i] + (threadIdx.x & 127);
-      if (row < p.S) {
-        const int tok = pos_of(p.layout, p.S, p.P, w.u, row);
+      if (row < sq.len) {
+        const int tok = sq.base + row * sq.stride;
         const size_t md = (static_cast<size_t>(w.bat) * p.H + w.head[i]) * p.N + tok;
         p.m[md] = -INFINITY;
         p.z[md] = 0.f;
@@ -244,34 +260,37 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_rows(&tq, sbase + L::kQ + i * L::kTile + c * L::kChunk, bar(kBarQ), p.layout, c,
-                   w.head[i], w.u, w.row0[i], w.bat);
+                   w.head[i], sq.chunk, w.row0[i], w.bat);
       int t = 0;
       for (int s = p.s_begin; s < p.s_end && ok; ++s) {
         const int b = shard_at(p, w.u, s);
-        const int nk = kv_tiles(p, b, w.qpos_max);
-        for (int kt = 0; kt < nk; ++kt, ++t) {
-          const int st = t & 1;
-          const uint32_t n = static_cast<uint32_t>(t >> 1);
-          if (t >= 2 && !bounded_wait(bar(kBarKE + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
-            ok = false;
-            break;
+        for (int ks = 0; ks < (ZIG ? 2 : 1) && ok; ++ks) {
+          const Seg sk = seg_of(p.layout, p.S, p.P, b, ks);
+          const int nk = kv_tiles(p, sk, w.qpos_max);
+          for (int kt = 0; kt < nk; ++kt, ++t) {
+            const int st = t & 1;
+            const uint32_t n = static_cast<uint32_t>(t >> 1);
+            if (t >= 2 && !bounded_wait(bar(kBarKE + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(kBarKF + st), L::kTile);
+  #pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_rows(&tk, sbase + L::kK + st * L::kTile + c * L::kChunk, bar(kBarKF + st),
+                       p.layout, c, w.g, sk.chunk, kt * 128, w.bat);
+            if (st) ++nk1; else ++nk0;
+            if (t >= 2 && !bounded_wait(bar(kBarVE + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(kBarVF + st), L::kTile);
+  #pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_rows(&tv, sbase + L::kV + st * L::kTile + c * L::kChunk, bar(kBarVF + st),
+                       p.layout, c, w.g, sk.chunk, kt * 128, w.bat);
+            if (st) ++nv1; else ++nv0;
           }
-          mbar_arrive_expect_tx(bar(kBarKF + st), L::kTile);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_rows(&tk, sbase + L::kK + st * L::kTile + c * L::kChunk, bar(kBarKF + st),
-                     p.layout, c, w.g, b, kt * 128, w.bat);
-          if (st) ++nk1; else ++nk0;
-          if (t >= 2 && !bounded_wait(bar(kBarVE + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(kBarVF + st), L::kTile);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_rows(&tv, sbase + L::kV + st * L::kTile + c * L::kChunk, bar(kBarVF + st),
-                     p.layout, c, w.g, b, kt * 128, w.bat);
-          if (st) ++nv1; else ++nv0;
         }
       }
       if (!ok) {
@@ -374,9 +393,9 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     // -------------------------------------------------------------- softmax
     const int i = warp >> 2;                 // sub-tile of this group
     const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter + 32)
-    const int row = w.row0[i] + quarter * 32 + lane;
-    const bool valid = row < p.S;
-    const int qpos = valid ? pos_of(p.layout, p.S, p.P, w.u, row) : -1;
+    const int row = w.row0[i] + quarter * 32 + lane;   // within the query segment
+    const bool valid = row < sq.len;
+    const int qpos = valid ? sq.base + row * sq.stride : -1;
     const int head = w.head[i];
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + i * 128 + lane_off;
@@ -419,115 +438,118 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     int t = 0;
     for (int s = p.s_begin; s < p.s_end && ok; ++s) {
       const int b = shard_at(p, w.u, s);
-      const int nk = kv_tiles(p, b, w.qpos_max);
-      for (int kt = 0; kt < nk; ++kt, ++t) {
-        const bool got = bounded_wait(bar(kBarSF + i), t & 1, p.timeout_ns, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        float sc[128];
-        {
-          uint32_t r[128];
-          tmem_ld_x128(tS, r);
-#pragma unroll
-          for (int j = 0; j < 128; ++j) sc[j] = __uint_as_float(r[j]);
-        }
-        // Causal and shard-tail mask: the visible keys of this tile are a prefix.
-        const int cnt = visible_prefix(p.layout, p.S, p.P, p.causal, b, kt * 128, 128, qpos);
-        if (__any_sync(0xffffffffu, cnt < 128)) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= cnt) sc[c] = -INFINITY;
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          mx0 = fmax3(mx0, sc[c], sc[c + 1]);
-          mx1 = fmax3(mx1, sc[c + 2], sc[c + 3]);
-          mx2 = fmax3(mx2, sc[c + 4], sc[c + 5]);
-          mx3 = fmax3(mx3, sc[c + 6], sc[c + 7]);
-        }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (m_tile > m_run) {
-          // exact rescale by alpha = exp(m_old - m_new) whenever the running max grows
-          if (m_run == -INFINITY) {
-            alpha = 0.f;            // nothing accumulated yet: the state is zero
-          } else {
-            alpha = ex2(m_run - m_tile);
-            rescale = true;
+      for (int ks = 0; ks < (ZIG ? 2 : 1) && ok; ++ks) {
+        const Seg sk = seg_of(p.layout, p.S, p.P, b, ks);
+        const int nk = kv_tiles(p, sk, w.qpos_max);
+        for (int kt = 0; kt < nk; ++kt, ++t) {
+          const bool got = bounded_wait(bar(kBarSF + i), t & 1, p.timeout_ns, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
           }
-          m_run = m_tile;
-        }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        const float2 cc = make_float2(c2, c2);
-        const float2 mneg = make_float2(-m_use, -m_use);
-        float2 za = make_float2(0.f, 0.f), zb = za, zc = za, zd = za;
-#pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          float2 x0 = ffma2(make_float2(sc[c], sc[c + 1]), cc, mneg);
-          float2 x1 = ffma2(make_float2(sc[c + 2], sc[c + 3]), cc, mneg);
-          float2 x2 = ffma2(make_float2(sc[c + 4], sc[c + 5]), cc, mneg);
-          float2 x3 = ffma2(make_float2(sc[c + 6], sc[c + 7]), cc, mneg);
-          x0 = make_float2(ex2(x0.x), ex2(x0.y));
-          x1 = make_float2(ex2(x1.x), ex2(x1.y));
-          x2 = make_float2(ex2(x2.x), ex2(x2.y));
-          x3 = make_float2(ex2(x3.x), ex2(x3.y));
-          za = fadd2(za, x0);
-          zb = fadd2(zb, x1);
-          zc = fadd2(zc, x2);
-          zd = fadd2(zd, x3);
-          sc[c] = x0.x; sc[c + 1] = x0.y; sc[c + 2] = x1.x; sc[c + 3] = x1.y;
-          sc[c + 4] = x2.x; sc[c + 5] = x2.y; sc[c + 6] = x3.x; sc[c + 7] = x3.y;
-        }
-        const float2 zs = fadd2(fadd2(za, zb), fadd2(zc, zd));
-        z_run = z_run * alpha + (zs.x + zs.y);
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(sc[h2 * 64 + 2 * j], sc[h2 * 64 + 2 * j + 1]);
-          tmem_st_x32(tS + h2 * 32, pk);
-        }
-        // Rescale this row's O by alpha before P V of this tile is issued (the
-        // MMA that produced O so far has completed: see the commit order above).
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float2 a2 = rescale ? make_float2(alpha, alpha) : make_float2(1.f, 1.f);
-#pragma unroll
-          for (int c = 0; c < D / 128 + (D % 128 ? 1 : 0); ++c) {
-            if (D >= 128) {
-              uint32_t r[128];
-              tmem_ld_x128(tO + c * 128, r);
-#pragma unroll
-              for (int j = 0; j < 128; j += 2) {
-                const float2 v = fmul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2);
-                r[j] = __float_as_uint(v.x);
-                r[j + 1] = __float_as_uint(v.y);
-              }
-              tmem_st_x128(tO + c * 128, r);
+          tc_fence_after_sync();
+          float sc[128];
+          {
+            uint32_t r[128];
+            tmem_ld_x128(tS, r);
+  #pragma unroll
+            for (int j = 0; j < 128; ++j) sc[j] = __uint_as_float(r[j]);
+          }
+          // Causal and segment-tail mask: the visible keys of this tile are a prefix.
+          const int cnt = seg_visible(sk, p.causal, kt * 128, 128, qpos);
+          if (__any_sync(0xffffffffu, cnt < 128)) {
+  #pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= cnt) sc[c] = -INFINITY;
+          }
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+  #pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            mx0 = fmax3(mx0, sc[c], sc[c + 1]);
+            mx1 = fmax3(mx1, sc[c + 2], sc[c + 3]);
+            mx2 = fmax3(mx2, sc[c + 4], sc[c + 5]);
+            mx3 = fmax3(mx3, sc[c + 6], sc[c + 7]);
+          }
+          const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (m_tile > m_run) {
+            // exact rescale by alpha = exp(m_old - m_new) whenever the running max grows
+            if (m_run == -INFINITY) {
+              alpha = 0.f;            // nothing accumulated yet: the state is zero
             } else {
+              alpha = ex2(m_run - m_tile);
+              rescale = true;
+            }
+            m_run = m_tile;
+          }
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+          const float2 cc = make_float2(c2, c2);
+          const float2 mneg = make_float2(-m_use, -m_use);
+          float2 za = make_float2(0.f, 0.f), zb = za, zc = za, zd = za;
 #pragma unroll
-              for (int c2i = 0; c2i < D / 32; ++c2i) {
-                uint32_t r[32];
-                tmem_ld_x32(tO + c2i * 32, r);
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
+          for (int c = 0; c < 128; c += 8) {
+            float2 x0 = ffma2(make_float2(sc[c], sc[c + 1]), cc, mneg);
+            float2 x1 = ffma2(make_float2(sc[c + 2], sc[c + 3]), cc, mneg);
+            float2 x2 = ffma2(make_float2(sc[c + 4], sc[c + 5]), cc, mneg);
+            float2 x3 = ffma2(make_float2(sc[c + 6], sc[c + 7]), cc, mneg);
+            x0 = make_float2(ex2(x0.x), ex2(x0.y));
+            x1 = make_float2(ex2(x1.x), ex2(x1.y));
+            x2 = make_float2(ex2(x2.x), ex2(x2.y));
+            x3 = make_float2(ex2(x3.x), ex2(x3.y));
+            za = fadd2(za, x0);
+            zb = fadd2(zb, x1);
+            zc = fadd2(zc, x2);
+            zd = fadd2(zd, x3);
+            sc[c] = x0.x; sc[c + 1] = x0.y; sc[c + 2] = x1.x; sc[c + 3] = x1.y;
+            sc[c + 4] = x2.x; sc[c + 5] = x2.y; sc[c + 6] = x3.x; sc[c + 7] = x3.y;
+          }
+          const float2 zs = fadd2(fadd2(za, zb), fadd2(zc, zd));
+          z_run = z_run * alpha + (zs.x + zs.y);
+  #pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[32];
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(sc[h2 * 64 + 2 * j], sc[h2 * 64 + 2 * j + 1]);
+            tmem_st_x32(tS + h2 * 32, pk);
+          }
+          // Rescale this row's O by alpha before P V of this tile is issued (the
+          // MMA that produced O so far has completed: see the commit order above).
+          if (__any_sync(0xffffffffu, rescale)) {
+            const float2 a2 = rescale ? make_float2(alpha, alpha) : make_float2(1.f, 1.f);
+  #pragma unroll
+            for (int c = 0; c < D / 128 + (D % 128 ? 1 : 0); ++c) {
+              if (D >= 128) {
+                uint32_t r[128];
+                tmem_ld_x128(tO + c * 128, r);
+  #pragma unroll
+                for (int j = 0; j < 128; j += 2) {
                   const float2 v = fmul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2);
                   r[j] = __float_as_uint(v.x);
                   r[j + 1] = __float_as_uint(v.y);
                 }
-                tmem_st_x32(tO + c2i * 32, r);
+                tmem_st_x128(tO + c * 128, r);
+              } else {
+  #pragma unroll
+                for (int c2i = 0; c2i < D / 32; ++c2i) {
+                  uint32_t r[32];
+                  tmem_ld_x32(tO + c2i * 32, r);
+  #pragma unroll
+                  for (int j = 0; j < 32; j += 2) {
+                    const float2 v = fmul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2);
+                    r[j] = __float_as_uint(v.x);
+                    r[j + 1] = __float_as_uint(v.y);
+                  }
+                  tmem_st_x32(tO + c2i * 32, r);
+                }
               }
             }
           }
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarPF + i));
         }
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPF + i));
       }
     }
 
@@ -598,13 +620,20 @@ cudaError_t launch_d(const RingParams& p, const CUtensorMap& tq, const CUtensorM
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done.load() & bit)) {
-    e = cudaFuncSetAttribute(ring_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(ring_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ring_tc_kernel<D, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
   const long long grid = static_cast<long long>(p.B) * p.G * p.units_per_bg;
   if (grid <= 0) return cudaSuccess;
-  ring_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tk, tv);
+  if (p.layout == kZigzag)
+    ring_tc_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tk, tv);
+  else
+    ring_tc_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 

@@ -58,7 +58,8 @@ FAKE = ctypes.c_void_p(0x10000)      # aligned, never dereferenced: checks fail 
     (dict(batch=0), _lib.RA_ERR_INVALID_ARG),
     (dict(P=0), _lib.RA_ERR_INVALID_ARG),
     (dict(P=512), _lib.RA_ERR_INVALID_ARG),               # P > N
-    (dict(layout=2), _lib.RA_ERR_INVALID_ARG),
+    (dict(layout=3), _lib.RA_ERR_INVALID_ARG),
+    (dict(layout=2, seqlen=258, P=2), _lib.RA_ERR_INVALID_ARG),   # zigzag: 258 % 4 != 0
     (dict(causal=2), _lib.RA_ERR_INVALID_ARG),
     (dict(scale=-1.0), _lib.RA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), _lib.RA_ERR_INVALID_ARG),
@@ -88,9 +89,11 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.ring_attn_selftest_timeout(0, None) == _lib.RA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
-@pytest.mark.parametrize("N,P", [(8, 4), (12, 3), (1024, 16), (96, 96), (7, 1)])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
+@pytest.mark.parametrize("N,P", [(8, 4), (12, 3), (1024, 16), (96, 96), (7, 1), (10, 1)])
 def test_host_shard_map_bit_exact_vs_oracle(lib, layout, N, P):
+    if layout == "zigzag" and N % (2 * P):
+        pytest.skip("zigzag needs N divisible by 2P")
     from oracle import shardmap as OS
     import online_softmax_merge_gb300 as ra
     got = ra.shard_map(layout, N, P)
@@ -102,6 +105,7 @@ def test_host_shard_map_rejects_bad_sizes(lib):
     arr = (ctypes.c_int32 * 10)()
     assert lib.ring_attn_shard_map(0, 10, 3, arr, arr, arr) == _lib.RA_ERR_INVALID_ARG
     assert lib.ring_attn_shard_map(5, 10, 2, arr, arr, arr) == _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_shard_map(2, 10, 2, arr, arr, arr) == _lib.RA_ERR_INVALID_ARG  # 10 % 4
     assert lib.ring_attn_shard_map(0, 10, 2, None, arr, arr) == _lib.RA_ERR_INVALID_ARG
 
 

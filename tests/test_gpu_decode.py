@@ -36,6 +36,8 @@ CASES = [
     (1, 2 * 300, 6, 2, 64, 2, "contiguous", False, 5, 0),
     (2, 5000, 2, 1, 64, 1, "contiguous", True, 4, None),         # P = 1, ragged chunks
     (1, 2 * 4500, 16, 1, 128, 2, "striped", True, 3, None),      # 48 rows: two row groups
+    (1, 4 * 2600, 8, 2, 128, 2, "zigzag", True, 2, 5000),        # zigzag, chunks span halves
+    (2, 8 * 512, 4, 1, 64, 4, "zigzag", True, 1, None),
 ]
 
 

@@ -42,6 +42,11 @@ CASES = [
     ("s1-every-token-a-shard", 1, 64, 2, 1, 128, 64, "striped", True),
     ("s1-contig", 1, 48, 2, 2, 64, 48, "contiguous", True),
     ("tiny", 1, 5, 2, 2, 128, 1, "contiguous", False),
+    ("zigzag-causal-tail", 1, 8 * (128 + 40), 4, 2, 128, 4, "zigzag", True),
+    ("zigzag-full-aligned", 1, 4 * 256, 4, 2, 128, 2, "zigzag", False),
+    ("zigzag-mha-d64", 2, 6 * 100, 3, 3, 64, 3, "zigzag", True),
+    ("zigzag-p1", 1, 2 * 300, 2, 1, 128, 1, "zigzag", True),
+    ("zigzag-s2", 1, 64, 4, 2, 128, 32, "zigzag", True),
 ]
 
 
@@ -56,13 +61,14 @@ def test_fwd_matches_oracle(case):
 
 # Two GPU results are each within TOL of the exact value, so within 2 TOL of
 # each other (two bf16 roundings of nearly equal values can differ by an ulp).
-def test_contiguous_equals_striped_on_same_tensors():
+def test_contiguous_equals_striped_and_zigzag_on_same_tensors():
     w = Workload("cs", 1, 8 * 192, 4, 2, 128, 8, "contiguous", True, seed=5)
     q, k, v, o1, l1 = _run(w)
-    o2, l2 = ra.fwd(q, k, v, w.P, "striped", True)
-    torch.cuda.synchronize()
-    assert float((o1.float() - o2.float()).abs().max()) <= 2 * TOL_O
-    assert float((l1 - l2).abs().max()) <= 2 * TOL_LSE
+    for layout in ("striped", "zigzag"):
+        o2, l2 = ra.fwd(q, k, v, w.P, layout, True)
+        torch.cuda.synchronize()
+        assert float((o1.float() - o2.float()).abs().max()) <= 2 * TOL_O
+        assert float((l1 - l2).abs().max()) <= 2 * TOL_LSE
 
 
 def test_p_invariance_and_p1_is_plain_attention():

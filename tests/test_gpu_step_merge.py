@@ -30,6 +30,7 @@ STEP_CASES = [
     Workload("st-striped", 1, 4 * (2 * 128 + 24), 4, 2, 128, 4, "striped", True, 22),
     Workload("st-full-d64", 1, 3 * 200, 2, 1, 64, 3, "contiguous", False, 23),
     Workload("st-mha", 2, 2 * 300, 3, 3, 128, 2, "striped", True, 24),
+    Workload("st-zigzag", 1, 6 * 200, 4, 2, 128, 3, "zigzag", True, 30),
 ]
 
 
@@ -72,7 +73,7 @@ def test_step_state_follows_oracle_recurrence(w, impl):
     assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 def test_steps_in_any_order_give_dense_result(layout):
     w = Workload("order", 1, 5 * 160, 4, 2, 128, 5, layout, True, 25)
     q, k, v = _inputs(w)
@@ -143,7 +144,7 @@ def test_merge_matches_oracle(n, B, N, H, d):
     assert np.all(host32(o)[0, :3, 0] == 0)
 
 
-@pytest.mark.parametrize("layout", ["contiguous", "striped"])
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
 def test_merge_of_oracle_shard_partials_equals_dense(layout):
     w = Workload("mp", 1, 4 * 96, 4, 2, 128, 4, layout, True, 28)
     q, k, v = make_qkv(w)
