@@ -22,6 +22,8 @@
 //    query row reads its S row from TMEM, applies the causal / tail mask, updates
 //    the running max and denominator in fp32, rescales its O row in TMEM when the
 //    max grows, and writes P = exp(S - m) as bf16 back over S for the P·V MMA;
+//    P is published in two halves (keys 0-63, then 64-127), so the first four
+//    P·V MMAs run while the softmax is still on the second half;
 //  * the MMA order PV_0(t), S_0(t+1), PV_1(t), S_1(t+1) lets each softmax group
 //    work while the tensor core serves the other group, and the commit that
 //    signals S_i(t+1) also proves PV_i(t) finished, so O_i is stable when read.
@@ -62,8 +64,8 @@ struct Smem {
 };
 
 enum : int {
-  kBarQ = 0, kBarKF = 1, kBarKE = 3, kBarVF = 5, kBarVE = 7, kBarSF = 9, kBarPF = 11,
-  kBarOF = 13, kBarDrain = 15, kNumBars = 16
+  kBarQ = 0, kBarKF = 1, kBarKE = 3, kBarVF = 5, kBarVE = 7, kBarSF = 9, kBarOF = 11,
+  kBarDrain = 13, kBarPF = 14, kNumBars = 18   // kBarPF + 2*i + h: half h of P_i
 };
 
 struct Unit {
@@ -172,11 +174,12 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 // 64-column chunks Smem::kChunk apart, which v_desc carries as its leading
 // byte offset).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                              int h, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
+  for (int k4 = 0; k4 < 4; ++k4) {
+    const int kk = h * 4 + k4;
     mma_ts(d_tmem, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
            (kk > 0 || accumulate) ? 1u : 0u);
   }
@@ -229,8 +232,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
-    mbar_init(bar(kBarPF + 0), 4);   // one arrival per softmax warp
-    mbar_init(bar(kBarPF + 1), 4);
+    for (int x = 0; x < 4; ++x) mbar_init(bar(kBarPF + x), 4);   // one arrival per softmax warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -347,8 +349,15 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
           break;
         }
         tc_fence_after_sync();
+        if (elect_one()) issue_pv_half<D>(tO0, tS0, vs, 0, acc);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 1), t & 1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
         if (elect_one()) {
-          issue_pv<D>(tO0, tS0, vs, acc);
+          issue_pv_half<D>(tO0, tS0, vs, 1, acc);
           if (!has_next) mma_commit(bar(kBarOF + 0));
         }
         __syncwarp();
@@ -364,13 +373,20 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
           }
           __syncwarp();
         }
-        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 1), t & 1, p.timeout_ns, abort_flag))) {
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 2), t & 1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) issue_pv_half<D>(tO1, tS1, vs, 0, acc);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 3), t & 1, p.timeout_ns, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         if (elect_one()) {
-          issue_pv<D>(tO1, tS1, vs, acc);
+          issue_pv_half<D>(tO1, tS1, vs, 1, acc);
           mma_commit(bar(kBarVE + st));
           if (!has_next) mma_commit(bar(kBarOF + 1));
           if (has_next) {
@@ -486,69 +502,59 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
           const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
           const float2 cc = make_float2(c2, c2);
           const float2 mneg = make_float2(-m_use, -m_use);
-          float2 za = make_float2(0.f, 0.f), zb = za, zc = za, zd = za;
+          float z_tile = 0.f;
 #pragma unroll
-          for (int c = 0; c < 128; c += 8) {
-            float2 x0 = ffma2(make_float2(sc[c], sc[c + 1]), cc, mneg);
-            float2 x1 = ffma2(make_float2(sc[c + 2], sc[c + 3]), cc, mneg);
-            float2 x2 = ffma2(make_float2(sc[c + 4], sc[c + 5]), cc, mneg);
-            float2 x3 = ffma2(make_float2(sc[c + 6], sc[c + 7]), cc, mneg);
-            x0 = make_float2(ex2(x0.x), ex2(x0.y));
-            x1 = make_float2(ex2(x1.x), ex2(x1.y));
-            x2 = make_float2(ex2(x2.x), ex2(x2.y));
-            x3 = make_float2(ex2(x3.x), ex2(x3.y));
-            za = fadd2(za, x0);
-            zb = fadd2(zb, x1);
-            zc = fadd2(zc, x2);
-            zd = fadd2(zd, x3);
-            sc[c] = x0.x; sc[c + 1] = x0.y; sc[c + 2] = x1.x; sc[c + 3] = x1.y;
-            sc[c + 4] = x2.x; sc[c + 5] = x2.y; sc[c + 6] = x3.x; sc[c + 7] = x3.y;
-          }
-          const float2 zs = fadd2(fadd2(za, zb), fadd2(zc, zd));
-          z_run = z_run * alpha + (zs.x + zs.y);
-  #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
+            // probabilities of keys [64 h2, 64 h2 + 64), stored as P columns [32 h2, 32 h2 + 32)
+            float2 za = make_float2(0.f, 0.f), zb = za, zc = za, zd = za;
+#pragma unroll
+            for (int c = h2 * 64; c < h2 * 64 + 64; c += 8) {
+              float2 x0 = ffma2(make_float2(sc[c], sc[c + 1]), cc, mneg);
+              float2 x1 = ffma2(make_float2(sc[c + 2], sc[c + 3]), cc, mneg);
+              float2 x2 = ffma2(make_float2(sc[c + 4], sc[c + 5]), cc, mneg);
+              float2 x3 = ffma2(make_float2(sc[c + 6], sc[c + 7]), cc, mneg);
+              x0 = make_float2(ex2(x0.x), ex2(x0.y));
+              x1 = make_float2(ex2(x1.x), ex2(x1.y));
+              x2 = make_float2(ex2(x2.x), ex2(x2.y));
+              x3 = make_float2(ex2(x3.x), ex2(x3.y));
+              za = fadd2(za, x0);
+              zb = fadd2(zb, x1);
+              zc = fadd2(zc, x2);
+              zd = fadd2(zd, x3);
+              sc[c] = x0.x; sc[c + 1] = x0.y; sc[c + 2] = x1.x; sc[c + 3] = x1.y;
+              sc[c + 4] = x2.x; sc[c + 5] = x2.y; sc[c + 6] = x3.x; sc[c + 7] = x3.y;
+            }
+            const float2 zs = fadd2(fadd2(za, zb), fadd2(zc, zd));
+            z_tile += zs.x + zs.y;
             uint32_t pk[32];
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(sc[h2 * 64 + 2 * j], sc[h2 * 64 + 2 * j + 1]);
             tmem_st_x32(tS + h2 * 32, pk);
-          }
-          // Rescale this row's O by alpha before P V of this tile is issued (the
-          // MMA that produced O so far has completed: see the commit order above).
-          if (__any_sync(0xffffffffu, rescale)) {
-            const float2 a2 = rescale ? make_float2(alpha, alpha) : make_float2(1.f, 1.f);
-  #pragma unroll
-            for (int c = 0; c < D / 128 + (D % 128 ? 1 : 0); ++c) {
-              if (D >= 128) {
-                uint32_t r[128];
-                tmem_ld_x128(tO + c * 128, r);
-  #pragma unroll
-                for (int j = 0; j < 128; j += 2) {
-                  const float2 v = fmul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2);
-                  r[j] = __float_as_uint(v.x);
-                  r[j + 1] = __float_as_uint(v.y);
-                }
-                tmem_st_x128(tO + c * 128, r);
-              } else {
-  #pragma unroll
-                for (int c2i = 0; c2i < D / 32; ++c2i) {
+            if (h2 == 0) {
+              // Rescale this row's O by alpha before any P V MMA of this tile is
+              // issued (the MMA that produced O so far has completed).
+              if (__any_sync(0xffffffffu, rescale)) {
+                const float2 a2 = rescale ? make_float2(alpha, alpha) : make_float2(1.f, 1.f);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
                   uint32_t r[32];
-                  tmem_ld_x32(tO + c2i * 32, r);
-  #pragma unroll
+                  tmem_ld_x32(tO + c * 32, r);
+#pragma unroll
                   for (int j = 0; j < 32; j += 2) {
                     const float2 v = fmul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), a2);
                     r[j] = __float_as_uint(v.x);
                     r[j + 1] = __float_as_uint(v.y);
                   }
-                  tmem_st_x32(tO + c2i * 32, r);
+                  tmem_st_x32(tO + c * 32, r);
                 }
               }
             }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarPF + 2 * i + h2));
           }
-          tmem_st_wait();
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarPF + i));
+          z_run = z_run * alpha + z_tile;
         }
       }
     }
