@@ -23,18 +23,19 @@ each function by page title and section:
     softmax accumulation actually does across rounds", "The causal masking
     complication".
   * Transformer Math "Ring Attention" (aicassindra.com): "The mechanism,
-    compressed" and "The ring is a prefill algorithm" (the rescale-and-add
-    merge of P partial states).
+    compressed", "The ring is a prefill algorithm" (the rescale-and-add
+    merge of P partial states) and "The backward pass costs a second ring".
 
 Modules:
   attention  dense softmax attention, the plain definition (+ sampled rows)
   ring       the ring recurrence over P virtual shards, fold by fold
   merge      merge of normalised partials (O_p, LSE_p) and finalize (m, z, y)
   shardmap   shard ownership maps, causal visibility, tile classes (brute force)
+  backward   dQ, dK, dV of softmax attention (chain rule) and the backward ring
 
 Every function here is pinned by tests under tests/ (test_oracle_*.py) against
 values the pages print, closed forms, library routines for special cases,
 invariants and brute force on tiny inputs. No function is "parity unpinned".
 """
 
-from . import attention, ring, merge, shardmap  # noqa: F401
+from . import attention, ring, merge, shardmap, backward  # noqa: F401
