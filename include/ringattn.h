@@ -32,7 +32,8 @@
  *  ("Ring Attention: what the near-infinite context paper actually says",
  *  "The causal masking complication").
  *
- *  Pointers named q,k,v,o,lse,m,z,y,o_parts,lse_parts are DEVICE pointers,
+ *  Pointers named q,k,v,o,lse,m,z,y,o_parts,lse_parts,dout,dq,dk,dv,workspace
+ *  are DEVICE pointers,
  *  allocated and owned by the caller, 16-byte aligned. The library allocates
  *  no device memory; it keeps one status word in static device memory per GPU.
  *  `stream` is a cudaStream_t (NULL = legacy default stream); every call that
@@ -188,6 +189,34 @@ size_t ring_attn_decode_workspace_bytes(const ra_problem* p, int32_t n_q);
 ra_status ring_attn_decode_noalloc(const ra_problem* p, int32_t n_q, int32_t q_pos0,
                                    const void* q, const void* k, const void* v, void* o,
                                    float* lse, void* stream);
+
+/* Backward of the full ring forward: dQ, dK, dV for an upstream gradient dO,
+ * from the forward's inputs and its saved output O and LSE. The K/V blocks
+ * circulate a second time carrying their accumulating dK/dV, each query shard
+ * adds its contribution as a block passes, and the score blocks are recomputed
+ * from the saved per-row statistics rather than stored (Transformer Math "Ring
+ * Attention" (aicassindra), "The backward pass costs a second ring"). The ring
+ * runs in the reverse direction: at backward step s = 0..P-1 virtual device u
+ * holds block (u + s) mod P ("Ring Attention: what the near-infinite context
+ * paper actually says", "Production tradeoffs no one mentions in the benchmark
+ * post"). With S = scale Q K^T (causal mask as in the forward),
+ * A = exp(S - LSE) and D = rowsum(dO * O) per query row:
+ *     dV = A^T dO,  dS = A * (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q;
+ * a kv head's dK, dV sum over the query heads that read it. A row with
+ * LSE = -inf contributes nothing. Probabilities and dS are rounded to bf16 for
+ * the tensor-core products; accumulation is fp32; dq, dk, dv are written as
+ * bf16 (round to nearest even), every element overwritten.
+ * q, o, dout [B, N, H, d] bf16, k, v [B, N, G, d] bf16, lse [B, H, N] fp32 in;
+ * dq [B, N, H, d], dk, dv [B, N, G, d] bf16 out (device). workspace:
+ * caller-owned device memory of at least ring_attn_bwd_workspace_bytes(p)
+ * bytes, 16-byte aligned, overwritten. Three launches on stream. */
+ra_status ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                        void* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ring_attn_bwd needs for this problem (0 if the problem is
+ * invalid): 1 KiB per 128-row query tile of every (batch, head). Pure host code. */
+size_t ring_attn_bwd_workspace_bytes(const ra_problem* p);
 
 /* Shard ownership on the HOST: owner[t], local[t] for t < N and
  * token_of[u*S + i] (S = N/P) for the given layout. Pure host code; host

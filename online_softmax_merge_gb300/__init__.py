@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import (LAYOUTS, RA_ERR_CUDA, RA_ERR_INVALID_ARG, RA_ERR_TIMEOUT,  # noqa: F401
                    RA_ERR_UNSUPPORTED, RA_OK, TILE, RingAttnError, check, load)
 
-__all__ = ["fwd", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
+__all__ = ["fwd", "bwd", "bwd_workspace_bytes", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
            "tile_classes", "mask", "last_error", "selftest_timeout", "problem", "RingAttnError",
            "empty_state", "LAYOUTS", "TILE"]
 
@@ -84,6 +84,46 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str =
         check("ring_attn_fwd", lib.ring_attn_fwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v),
                                                  _ptr(out), _ptr(lse), _stream(q.device)))
     return out, lse
+
+
+def bwd_workspace_bytes(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int,
+                        P: int, layout: str = "contiguous", causal: bool = True) -> int:
+    """Workspace bytes ring_attn_bwd needs (ring_attn_bwd_workspace_bytes)."""
+    lib = load()
+    pr = problem(batch, seqlen, heads, kv_heads, head_dim, P, causal, layout)
+    return int(lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr)))
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, P: int, layout: str = "contiguous", causal: bool = True,
+        scale: float = 0.0, dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+        dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Backward ring (ring_attn_bwd): gradients of the forward for upstream gradient
+    dout, from the forward's saved o and lse. Returns (dq, dk, dv)."""
+    lib = load()
+    pr, (B, N, H, G, d) = _qkv_problem(q, k, v, P, layout, causal, scale)
+    _need(o, "o", torch.bfloat16, (B, N, H, d))
+    _need(lse, "lse", torch.float32, (B, H, N))
+    _need(dout, "dout", torch.bfloat16, (B, N, H, d))
+    need = int(lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16) // 4, dtype=torch.float32, device=q.device)
+    _need(workspace, "workspace", torch.float32)
+    if dq is None:
+        dq = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+    if dk is None:
+        dk = torch.empty((B, N, G, d), dtype=torch.bfloat16, device=q.device)
+    if dv is None:
+        dv = torch.empty((B, N, G, d), dtype=torch.bfloat16, device=q.device)
+    _need(dq, "dq", torch.bfloat16, (B, N, H, d))
+    _need(dk, "dk", torch.bfloat16, (B, N, G, d))
+    _need(dv, "dv", torch.bfloat16, (B, N, G, d))
+    with torch.cuda.device(q.device):
+        check("ring_attn_bwd", lib.ring_attn_bwd(
+            ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+            ctypes.c_size_t(workspace.numel() * 4), _stream(q.device)))
+    return dq, dk, dv
 
 
 def decode_workspace_bytes(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int,

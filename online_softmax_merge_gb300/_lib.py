@@ -36,6 +36,8 @@ SIGNATURES = {
     "ring_attn_decode": (_i32, [_PP, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "ring_attn_decode_workspace_bytes": (ctypes.c_size_t, [_PP, _i32]),
     "ring_attn_decode_noalloc": (_i32, [_PP, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ring_attn_bwd": (_i32, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "ring_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_PP]),
     "ring_attn_shard_map": (_i32, [_i32, _i32, _i32, _vp, _vp, _vp]),
     "ring_attn_shard_map_device": (_i32, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "ring_attn_tile_classes": (_i32, [_PP, _i32, _i32, _vp, _vp]),

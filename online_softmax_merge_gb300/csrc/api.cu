@@ -213,6 +213,15 @@ size_t decode_workspace(const ra_problem* pr, int32_t n_q) {
   return parts * rows * (static_cast<size_t>(pr->head_dim) + 1) * sizeof(float);
 }
 
+// Backward statistics workspace: 256 floats per (batch, head, chunk, 128-row tile).
+size_t bwd_workspace(const ra_problem* pr) {
+  const int S = pr->seqlen / pr->P;
+  const int X = pr->layout == RA_LAYOUT_ZIGZAG ? 2 * pr->P : pr->P;
+  const int L = pr->layout == RA_LAYOUT_ZIGZAG ? S / 2 : S;
+  const size_t nt = static_cast<size_t>((L + 127) / 128);
+  return static_cast<size_t>(pr->batch) * pr->heads * X * nt * 256 * sizeof(float);
+}
+
 }  // namespace
 
 extern "C" {
@@ -376,6 +385,66 @@ ra_status ring_attn_mask(const ra_problem* pr, int32_t u, int32_t b, uint8_t* ma
 size_t ring_attn_decode_workspace_bytes(const ra_problem* pr, int32_t n_q) {
   if (check_problem(pr) != RA_OK || n_q < 1) return 0;
   return decode_workspace(pr, n_q);
+}
+
+size_t ring_attn_bwd_workspace_bytes(const ra_problem* pr) {
+  if (check_problem(pr) != RA_OK) return 0;
+  return bwd_workspace(pr);
+}
+
+ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                        void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  const void* in[] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
+  for (const void* ptr : in)
+    if (ptr == nullptr || !aligned16(ptr)) return RA_ERR_INVALID_ARG;
+  if (workspace_bytes < bwd_workspace(pr)) return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  RingParams f;
+  fill_params(pr, &f);
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = f.B;
+  p.N = f.N;
+  p.H = f.H;
+  p.G = f.G;
+  p.D = f.D;
+  p.S = f.S;
+  p.P = f.P;
+  p.layout = f.layout;
+  p.causal = f.causal;
+  p.X = f.X;
+  p.L = f.L;
+  p.nt = f.nq;
+  p.scale = f.scale;
+  p.scale_log2 = f.scale_log2;
+  p.timeout_ns = f.timeout_ns;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.ws = static_cast<float*>(workspace);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = d->status;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // zigzag tiles by chunk: the contiguous view with X = 2P chunks of L = S/2 tokens
+  const int ml = p.layout == kZigzag ? kContiguous : p.layout;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!encode_rows(&tq, q, p.B, p.N, p.H, p.D, p.L, p.X, ml) ||
+      !encode_rows(&tdo, dout, p.B, p.N, p.H, p.D, p.L, p.X, ml) ||
+      !encode_rows(&tk, k, p.B, p.N, p.G, p.D, p.L, p.X, ml) ||
+      !encode_rows(&tv, v, p.B, p.N, p.G, p.D, p.L, p.X, ml))
+    return RA_ERR_CUDA;
+  if ((st = launch_result(launch_bwd_prep(p, s))) != RA_OK) return st;
+  if ((st = launch_result(launch_bwd_dkdv(p, tq, tdo, tk, tv, s))) != RA_OK) return st;
+  return launch_result(launch_bwd_dq(p, tq, tdo, tk, tv, s));
 }
 
 ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, const void* q,

@@ -1,0 +1,981 @@
+// Backward of the ring on sm_103a: dQ, dK, dV of softmax attention over P
+// virtual shards, from the forward's saved output O and LSE.
+//
+// What it computes — Transformer Math "Ring Attention" (aicassindra), "The
+// backward pass costs a second ring": the K/V blocks circulate a second time,
+// carrying their accumulating dK/dV, and every query shard they pass adds its
+// contribution; scores are rebuilt from the saved per-row statistics instead of
+// being stored. The gradients flow in the reverse direction ("Ring Attention:
+// what the near-infinite context paper actually says", "Production tradeoffs"):
+// at backward step s virtual device u holds block (u + s) mod P. With
+// S = scale Q K^T (causal mask on global positions), A = exp(S - LSE) and
+// D = rowsum(dO * O) of each query row:
+//     dV_b += A^T dO_u,   dS = A * (dO_u V_b^T - D_u),
+//     dQ_u += scale dS K_b,   dK_b += scale dS^T Q_u.
+//
+// How, on one GB300 SM. Three launches:
+//  * bwd_prep: D and LSE * log2(e) of every query row, written per 128-row tile
+//    (1 KiB each) so that a kernel fetches a tile's statistics in one bulk copy;
+//  * bwd_dkdv: a CTA owns one 128-key tile of one kv head — the circulating
+//    block — and meets the query tiles of every query head of its group, shard by
+//    shard in the reverse ring order u = (b - s) mod P, skipping tiles the causal
+//    mask leaves empty. dK and dV stay in TMEM for the whole walk;
+//  * bwd_dq: a CTA owns one 128-row query tile of one head and walks the key
+//    tiles of blocks b = (u + s) mod P; dQ stays in TMEM.
+// Both tensor-core kernels have 10 warps: warp 9 streams two tiles per step
+// through two shared-memory stages with TMA, warp 8 issues the tcgen05 MMAs
+// (one elected lane of a warp-uniform loop), and warps 0-7 are the element-wise
+// workers — warp w reads TMEM lane quarter w % 4 and score columns
+// [64 (w / 4), 64 (w / 4) + 64), so no row needs a reduction across threads.
+// Per step, the workers turn the score tile into A (phase 1) and dP into dS
+// (phase 2), each written back to TMEM as bf16 for the MMAs that take them as
+// the TMEM operand.
+//
+// dK/dV kernel, per query tile t (TMEM: dK [0,D), dV [D,2D), S^T [256,384),
+// dP^T [384,512)):  MMA order  dP^T(t) | dV += A^T(t) dO(t) | S^T(t+1) |
+// dK += dS^T(t) Q(t) | dP^T(t+1) ...  so the workers' phase 1 overlaps dP^T(t)
+// and phase 2 overlaps dV(t) and S^T(t+1).
+// dQ kernel, per key tile t (TMEM: S [0,128), dP [128,256), dQ [256,256+D)):
+// MMA order  dP(t) | S(t+1) | dQ += dS(t) K(t) | dP(t+1) ...
+// The tensor core runs these in issue order, so an MMA that overwrites a TMEM
+// region is always behind the MMAs that read it; the workers signal when they
+// have read a region into registers.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <atomic>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "shardmap.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr int kWorkers = 8;                   // element-wise warps
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s to let in-flight copies land on abort
+constexpr int kStatBytes = 1024;              // one tile's statistics: 128 x (LSE*log2e, D)
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kChunk = 128 * 128;          // 128 rows x 64 bf16 (128 B, swizzled)
+  static constexpr int kTile = (D / 64) * kChunk;   // one [128 x D] bf16 tile
+  static constexpr int kFix = 0;                    // two stationary tiles
+  static constexpr int kStage = 2 * kTile;          // two stages of two streamed tiles
+  static constexpr int kStats = 6 * kTile;          // dK/dV kernel: statistics, two stages
+  static constexpr int kBar = kStats + 2 * kStatBytes;
+  static constexpr int kBytes = kBar + 256;
+  // One CTA per SM: it owns all 512 TMEM columns.
+  static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+enum : int {
+  kBarFix = 0,      // stationary tiles landed
+  kBarFull = 1,     // + stage: streamed tiles landed
+  kBarEmpty = 3,    // + stage: MMAs done with the stage
+  kBarSF = 5,       // score tile in TMEM
+  kBarDPF = 6,      // dP tile in TMEM
+  kBarW1 = 7,       // workers: phase 1 done (8 arrivals)
+  kBarW2 = 8,       // workers: dS written (8 arrivals)
+  kBarDone = 9,     // every MMA of the CTA completed
+  kBarDrain = 10,
+  kNumBars = 11
+};
+
+__device__ __forceinline__ void record_failure(const BwdParams& p, volatile int* abort_flag) {
+  atomicCAS(p.status, 0, static_cast<int>(RA_ERR_TIMEOUT));
+  *abort_flag = 1;
+}
+
+// TMA box coordinates of 128 rows starting at row i0 of a chunk (see the
+// forward's tensor maps: (d, heads, L, X, B), or (d, heads, P, S, B) striped).
+__device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                         int layout, int dchunk, int head, int chunk, int i0,
+                                         int bat) {
+  if (layout == kStriped)
+    tma_load_5d(dst, map, bar, dchunk * 64, head, chunk, i0, bat);
+  else
+    tma_load_5d(dst, map, bar, dchunk * 64, head, i0, chunk, bat);
+}
+
+// D[tmem] = A B^T for two 128 x D tiles in shared memory (K-major, 128-byte
+// swizzled 64-column chunks): D/16 MMAs of 128 x 128 x 16.
+template <int D>
+__device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off =
+        static_cast<uint64_t>(((kk >> 2) * BwdSmem<D>::kChunk + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[tmem] (+)= A B with A [128 x 128] bf16 in TMEM — its 16-column K slices at
+// a_tmem + (kk / 4) * 64 + (kk % 4) * 8, i.e. two 32-column halves 64 columns
+// apart, as the workers write them — and B [128 x D] MN-major in shared memory
+// (16 rows = 2 KiB per MMA; the descriptor's leading offset is the chunk stride).
+template <int D>
+__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8,
+           b_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
+           (kk > 0 || accumulate) ? 1u : 0u);
+}
+
+__device__ __forceinline__ int ring_mod(int x, int P) {
+  x %= P;
+  return x < 0 ? x + P : x;
+}
+
+// Statistics tile of (batch, head, chunk, tile).
+__device__ __forceinline__ const float* stats_tile(const BwdParams& p, int bat, int h, int chunk,
+                                                   int tile) {
+  return p.ws + ((((static_cast<size_t>(bat) * p.H + h) * p.X + chunk) * p.nt + tile) << 8);
+}
+
+// --------------------------------------------------------------------------- prep
+// One row per TPR = D/8 threads (16 bytes of O and of dO each); warps advance
+// together so the shuffles always see whole groups.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
+  constexpr int TPR = D / 8;
+  constexpr int RPW = 32 / TPR;                       // rows per warp
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % TPR;
+  const long long tile_rows = static_cast<long long>(p.nt) * 128;
+  const long long rows = static_cast<long long>(p.B) * p.H * p.X * tile_rows;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long base = warp0 * RPW; base < rows; base += nwarps * RPW) {
+    const long long r = base + lane / TPR;
+    const bool in = r < rows;
+    long long rest = in ? r : 0;
+    const int ii = static_cast<int>(rest % tile_rows);
+    rest /= tile_rows;
+    const int c = static_cast<int>(rest % p.X);
+    rest /= p.X;
+    const int h = static_cast<int>(rest % p.H);
+    const int bat = static_cast<int>(rest / p.H);
+    const bool valid = in && ii < p.L;
+    float dsum = 0.f;
+    float l2 = INFINITY;
+    if (valid) {
+      const int pos = p.layout == kStriped ? ii * p.P + c : c * p.L + ii;
+      const size_t off = ((static_cast<size_t>(bat) * p.N + pos) * p.H + h) * D + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + off);
+      const uint4 b =
+          *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + off);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+        const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
+        dsum = fmaf(fa.x, fb.x, dsum);
+        dsum = fmaf(fa.y, fb.y, dsum);
+      }
+      const float l = p.lse[(static_cast<size_t>(bat) * p.H + h) * p.N + pos];
+      l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;   // a row with no key contributes 0
+    }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+    if (in && sub == 0) {
+      float* dst = p.ws + ((((static_cast<size_t>(bat) * p.H + h) * p.X + c) * p.nt + (ii >> 7)) << 8) +
+                   (ii & 127);
+      dst[0] = l2;
+      dst[128] = dsum;
+    }
+  }
+}
+
+// --------------------------------------------------------------------------- dK/dV
+struct KUnit {
+  int bat, g, b, kt;
+  Seg sk;       // segment of shard b that holds the key rows
+  int kpos0;    // global position of the tile's first key
+};
+
+__device__ __forceinline__ KUnit decode_kunit(const BwdParams& p, int idx) {
+  const int per_bg = p.X * p.nt;
+  const int bg = idx / per_bg;
+  const int r = idx - bg * per_bg;
+  // Earliest key positions first: under a causal mask they meet the most queries.
+  int c, kt;
+  if (p.layout == kStriped) {
+    kt = r / p.P;
+    c = r - kt * p.P;
+  } else {
+    c = r / p.nt;
+    kt = r - c * p.nt;
+  }
+  KUnit w;
+  w.bat = bg / p.G;
+  w.g = bg - w.bat * p.G;
+  w.kt = kt;
+  int seg = 0;
+  if (p.layout == kZigzag) {
+    w.b = c < p.P ? c : 2 * p.P - 1 - c;
+    seg = c < p.P ? 0 : 1;
+  } else {
+    w.b = c;
+  }
+  w.sk = seg_of(p.layout, p.S, p.P, w.b, seg);
+  w.kpos0 = w.sk.base + kt * 128 * w.sk.stride;
+  return w;
+}
+
+// First 128-row tile of query segment sq holding a query at or after position
+// kpos0 (every tile without the causal mask); p.nt if none.
+__device__ __forceinline__ int first_qtile(const BwdParams& p, const Seg& sq, int kpos0) {
+  if (!p.causal || kpos0 <= sq.base) return 0;
+  const int i = (kpos0 - sq.base + sq.stride - 1) / sq.stride;
+  return i >= sq.len ? p.nt : (i >> 7);
+}
+
+// Calls f(t, h, sq, qt) for every query tile the key tile meets, in the order
+// every role of the CTA walks: query heads of the group, then the reverse ring
+// u = (b - s) mod P, then segments and tiles. Stops when f returns false.
+template <bool ZIG, typename F>
+__device__ __forceinline__ void walk_qtiles(const BwdParams& p, const KUnit& w, F&& f) {
+  const int hpg = p.H / p.G;
+  int t = 0;
+  for (int hh = 0; hh < hpg; ++hh) {
+    const int h = w.g * hpg + hh;
+    for (int s = 0; s < p.P; ++s) {
+      const int u = ring_mod(w.b - s, p.P);
+      for (int qs = 0; qs < (ZIG ? 2 : 1); ++qs) {
+        const Seg sq = seg_of(p.layout, p.S, p.P, u, qs);
+        for (int qt = first_qtile(p, sq, w.kpos0); qt < p.nt; ++qt, ++t)
+          if (!f(t, h, sq, qt)) return;
+      }
+    }
+  }
+}
+
+template <int D, bool ZIG>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
+                const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kNumBars + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const KUnit w = decode_kunit(p, blockIdx.x);
+
+  int T = 0;
+  walk_qtiles<ZIG>(p, w, [&](int, int, const Seg&, int) { ++T; return true; });
+
+  if (T == 0) {
+    // No query sees these keys: their gradients are zero.
+    if (threadIdx.x < 128) {
+      const int j = w.kt * 128 + threadIdx.x;
+      if (j < w.sk.len) {
+        const int kpos = w.sk.base + j * w.sk.stride;
+        const size_t off = ((static_cast<size_t>(w.bat) * p.N + kpos) * p.G + w.g) * D;
+        uint4* a = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + off);
+        uint4* b = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + off);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) a[c] = b[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(kBarW1), kWorkers);
+    mbar_init(bar(kBarW2), kWorkers);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tensormap(&tq);
+    prefetch_tensormap(&tdo);
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t kColDK = 0, kColDV = D, kColS = 256, kColDP = 384;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      uint32_t nf0 = 0, nf1 = 0;   // loads issued per stage (for the drain on abort)
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(kBarFix), 2 * L::kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_rows(&tk, sbase + L::kFix + c * L::kChunk, bar(kBarFix), p.layout, c, w.g,
+                 w.sk.chunk, w.kt * 128, w.bat);
+        tma_rows(&tv, sbase + L::kFix + L::kTile + c * L::kChunk, bar(kBarFix), p.layout, c, w.g,
+                 w.sk.chunk, w.kt * 128, w.bat);
+      }
+      walk_qtiles<ZIG>(p, w, [&](int t, int h, const Seg& sq, int qt) {
+        const int st = t & 1;
+        const uint32_t n = static_cast<uint32_t>(t >> 1);
+        if (t >= 2 && !bounded_wait(bar(kBarEmpty + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          return false;
+        }
+        const uint32_t dst = sbase + L::kStage + st * 2 * L::kTile;
+        mbar_arrive_expect_tx(bar(kBarFull + st), 2 * L::kTile + kStatBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_rows(&tq, dst + c * L::kChunk, bar(kBarFull + st), p.layout, c, h, sq.chunk,
+                   qt * 128, w.bat);
+          tma_rows(&tdo, dst + L::kTile + c * L::kChunk, bar(kBarFull + st), p.layout, c, h,
+                   sq.chunk, qt * 128, w.bat);
+        }
+        bulk_load(sbase + L::kStats + st * kStatBytes, stats_tile(p, w.bat, h, sq.chunk, qt),
+                  kStatBytes, bar(kBarFull + st));
+        if (st) ++nf1; else ++nf0;
+        return true;
+      });
+      if (!ok) {
+        record_failure(p, abort_flag);
+        bounded_wait(bar(kBarFix), 0, kDrainNs, nullptr);
+        if (nf0) bounded_wait(bar(kBarFull), (nf0 - 1) & 1, kDrainNs, nullptr);
+        if (nf1) bounded_wait(bar(kBarFull + 1), (nf1 - 1) & 1, kDrainNs, nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    const uint32_t tDK = tmem + kColDK, tDV = tmem + kColDV;
+    const uint32_t tS = tmem + kColS, tDP = tmem + kColDP;
+    const uint64_t dK = smem_desc_sw128(sbase + L::kFix, 16, 1024);
+    const uint64_t dV = smem_desc_sw128(sbase + L::kFix + L::kTile, 16, 1024);
+    uint64_t dQk[2], dDOk[2], dQmn[2], dDOmn[2];
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      const uint32_t a = sbase + L::kStage + st * 2 * L::kTile;
+      dQk[st] = smem_desc_sw128(a, 16, 1024);
+      dDOk[st] = smem_desc_sw128(a + L::kTile, 16, 1024);
+      dQmn[st] = smem_desc_sw128(a, L::kChunk, 1024);
+      dDOmn[st] = smem_desc_sw128(a + L::kTile, L::kChunk, 1024);
+    }
+    bool ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarFix), 0, p.timeout_ns, abort_flag) &&
+                                      bounded_wait(bar(kBarFull), 0, p.timeout_ns, abort_flag));
+    if (ok) {
+      tc_fence_after_sync();
+      if (elect_one()) {
+        issue_ss<D>(tS, dK, dQk[0]);     // S^T(0) = K Q^T
+        mma_commit(bar(kBarSF));
+        issue_ss<D>(tDP, dV, dDOk[0]);   // dP^T(0) = V dO^T
+        mma_commit(bar(kBarDPF));
+      }
+      __syncwarp();
+    }
+    for (int t = 0; t < T && ok; ++t) {
+      const int st = t & 1, st1 = (t + 1) & 1;
+      const uint32_t ph1 = static_cast<uint32_t>((t + 1) >> 1) & 1;
+      const bool has_next = t + 1 < T;
+      const uint32_t par = static_cast<uint32_t>(t) & 1;
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW1), par, p.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (elect_one()) issue_ts<D>(tDV, tS, dDOmn[st], t > 0);   // dV += A^T dO
+      __syncwarp();
+      if (has_next) {
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarFull + st1), ph1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) {
+          issue_ss<D>(tS, dK, dQk[st1]);
+          mma_commit(bar(kBarSF));
+        }
+        __syncwarp();
+      }
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW2), par, p.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (elect_one()) {
+        issue_ts<D>(tDK, tDP, dQmn[st], t > 0);                    // dK += dS^T Q
+        mma_commit(bar(kBarEmpty + st));
+        if (has_next) {
+          issue_ss<D>(tDP, dV, dDOk[st1]);
+          mma_commit(bar(kBarDPF));
+        } else {
+          mma_commit(bar(kBarDone));
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      if (lane == 0) record_failure(p, abort_flag);
+      if (elect_one()) mma_commit(bar(kBarDrain));
+      __syncwarp();
+      bounded_wait(bar(kBarDrain), 0, kDrainNs, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- workers
+    const int quarter = warp & 3;      // TMEM lanes = key rows [32 quarter, 32 quarter + 32)
+    const int half = warp >> 2;        // query columns [64 half, 64 half + 64)
+    const int j = w.kt * 128 + quarter * 32 + lane;
+    const bool valid = j < w.sk.len;
+    const int kpos = w.sk.base + j * w.sk.stride;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + kColS + lane_off + half * 64;
+    const uint32_t tDP = tmem + kColDP + lane_off + half * 64;
+    const float* stats = reinterpret_cast<const float*>(smem + L::kStats);
+    const float2 cc = make_float2(p.scale_log2, p.scale_log2);
+    bool ok = true;
+    walk_qtiles<ZIG>(p, w, [&](int t, int, const Seg& sq, int qt) {
+      const uint32_t par = static_cast<uint32_t>(t) & 1;
+      const float* sl = stats + (t & 1) * 256 + half * 64;   // LSE*log2e; D at +128
+      // phase 1: A^T = exp2(S^T * scale * log2e - LSE * log2e), masked. The
+      // statistics came with the stage's TMA loads: observe that barrier too.
+      if (!__all_sync(0xffffffffu,
+                      bounded_wait(bar(kBarFull + (t & 1)), static_cast<uint32_t>(t >> 1) & 1,
+                                   p.timeout_ns, abort_flag) &&
+                          bounded_wait(bar(kBarSF), par, p.timeout_ns, abort_flag))) {
+        ok = false;
+        return false;
+      }
+      tc_fence_after_sync();
+      float a[64];
+      {
+        uint32_t r[64];
+        tmem_ld_x64(tS, r);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(sl + c);
+          const float2 x0 = ffma2(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cc,
+                                  make_float2(-l4.x, -l4.y));
+          const float2 x1 = ffma2(make_float2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
+                                  cc, make_float2(-l4.z, -l4.w));
+          a[c] = ex2(x0.x);
+          a[c + 1] = ex2(x0.y);
+          a[c + 2] = ex2(x1.x);
+          a[c + 3] = ex2(x1.y);
+        }
+      }
+      // Causal mask: the key at kpos sees the queries at or after it, a suffix
+      // of the tile's columns. (Columns past the chunk's end have LSE = +inf.)
+      int cf = 0;
+      if (p.causal) {
+        const int q0 = sq.base + qt * 128 * sq.stride;
+        cf = kpos <= q0 ? 0 : min(128, (kpos - q0 + sq.stride - 1) / sq.stride);
+        cf -= half * 64;
+      }
+      if (__any_sync(0xffffffffu, cf > 0)) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < cf) a[c] = 0.f;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(a[2 * c], a[2 * c + 1]);
+        tmem_st_x32(tS, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarW1));
+      // phase 2: dS^T = A^T * (dP^T - D)
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarDPF), par, p.timeout_ns, abort_flag))) {
+        ok = false;
+        return false;
+      }
+      tc_fence_after_sync();
+      {
+        uint32_t r[64];
+        tmem_ld_x64(tDP, r);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(sl + 128 + c);
+          const float2 e0 = fmul2(make_float2(a[c], a[c + 1]),
+                                  make_float2(__uint_as_float(r[c]) - d4.x,
+                                              __uint_as_float(r[c + 1]) - d4.y));
+          const float2 e1 = fmul2(make_float2(a[c + 2], a[c + 3]),
+                                  make_float2(__uint_as_float(r[c + 2]) - d4.z,
+                                              __uint_as_float(r[c + 3]) - d4.w));
+          pk[c >> 1] = pack_bf16x2(e0.x, e0.y);
+          pk[(c >> 1) + 1] = pack_bf16x2(e1.x, e1.y);
+        }
+        tmem_st_x32(tDP, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarW2));
+      return true;
+    });
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarDone), 0, p.timeout_ns, abort_flag));
+    if (!ok) {
+      if (lane == 0) record_failure(p, abort_flag);
+    } else {
+      tc_fence_after_sync();
+      // dK = scale * sum dS^T Q, dV = sum A^T dO: this warp writes columns
+      // [half * D/2, half * D/2 + D/2) of its key rows.
+      const size_t off = ((static_cast<size_t>(w.bat) * p.N + (valid ? kpos : 0)) * p.G + w.g) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which == 0 ? p.scale : 1.f;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which == 0 ? p.dk : p.dv) + off;
+        const uint32_t src = tmem + (which == 0 ? kColDK : kColDV) + lane_off;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          const int col = half * (D / 2) + c * 32;
+          uint32_t r[32];
+          tmem_ld_x32(src + col, r);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * mul, __uint_as_float(r[8 * q + 1]) * mul);
+              v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * mul, __uint_as_float(r[8 * q + 3]) * mul);
+              v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * mul, __uint_as_float(r[8 * q + 5]) * mul);
+              v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * mul, __uint_as_float(r[8 * q + 7]) * mul);
+              d4[q] = v;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------------------- dQ
+struct QUnit {
+  int bat, h, u, qt;
+  Seg sq;         // segment of shard u that holds the query rows
+  int qpos_max;   // latest global position among the tile's rows
+};
+
+__device__ __forceinline__ QUnit decode_qunit(const BwdParams& p, int idx) {
+  const int per_bh = p.X * p.nt;
+  const int bh = idx / per_bh;
+  const int r = idx - bh * per_bh;
+  // Latest query positions first: under a causal mask they see the most keys.
+  const int key = per_bh - 1 - r;
+  int c, qt;
+  if (p.layout == kStriped) {
+    qt = key / p.P;
+    c = key - qt * p.P;
+  } else {
+    c = key / p.nt;
+    qt = key - c * p.nt;
+  }
+  QUnit w;
+  w.bat = bh / p.H;
+  w.h = bh - w.bat * p.H;
+  w.qt = qt;
+  int seg = 0;
+  if (p.layout == kZigzag) {
+    w.u = c < p.P ? c : 2 * p.P - 1 - c;
+    seg = c < p.P ? 0 : 1;
+  } else {
+    w.u = c;
+  }
+  w.sq = seg_of(p.layout, p.S, p.P, w.u, seg);
+  const int last = min(qt * 128 + 127, w.sq.len - 1);
+  w.qpos_max = w.sq.base + last * w.sq.stride;
+  return w;
+}
+
+// Calls f(t, sk, kt) for every key tile the query tile sees, in the order every
+// role walks: blocks b = (u + s) mod P (the reverse ring), then segments, then
+// the visible prefix of tiles. Stops when f returns false.
+template <bool ZIG, typename F>
+__device__ __forceinline__ void walk_ktiles(const BwdParams& p, const QUnit& w, F&& f) {
+  int t = 0;
+  for (int s = 0; s < p.P; ++s) {
+    const int b = ring_mod(w.u + s, p.P);
+    for (int ks = 0; ks < (ZIG ? 2 : 1); ++ks) {
+      const Seg sk = seg_of(p.layout, p.S, p.P, b, ks);
+      const int nk = (seg_visible(sk, p.causal, 0, sk.len, w.qpos_max) + 127) >> 7;
+      for (int kt = 0; kt < nk; ++kt, ++t)
+        if (!f(t, sk, kt)) return;
+    }
+  }
+}
+
+template <int D, bool ZIG>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
+              const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kNumBars + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const QUnit w = decode_qunit(p, blockIdx.x);
+
+  int T = 0;
+  walk_ktiles<ZIG>(p, w, [&](int, const Seg&, int) { ++T; return true; });
+
+  if (T == 0) {
+    if (threadIdx.x < 128) {
+      const int i = w.qt * 128 + threadIdx.x;
+      if (i < w.sq.len) {
+        const int qpos = w.sq.base + i * w.sq.stride;
+        uint4* a = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) +
+                                            ((static_cast<size_t>(w.bat) * p.N + qpos) * p.H + w.h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(kBarW1), kWorkers);
+    mbar_init(bar(kBarW2), kWorkers);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tensormap(&tq);
+    prefetch_tensormap(&tdo);
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      uint32_t nf0 = 0, nf1 = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(kBarFix), 2 * L::kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_rows(&tq, sbase + L::kFix + c * L::kChunk, bar(kBarFix), p.layout, c, w.h,
+                 w.sq.chunk, w.qt * 128, w.bat);
+        tma_rows(&tdo, sbase + L::kFix + L::kTile + c * L::kChunk, bar(kBarFix), p.layout, c, w.h,
+                 w.sq.chunk, w.qt * 128, w.bat);
+      }
+      const int g = (w.h * p.G) / p.H;
+      walk_ktiles<ZIG>(p, w, [&](int t, const Seg& sk, int kt) {
+        const int st = t & 1;
+        const uint32_t n = static_cast<uint32_t>(t >> 1);
+        if (t >= 2 && !bounded_wait(bar(kBarEmpty + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          return false;
+        }
+        const uint32_t dst = sbase + L::kStage + st * 2 * L::kTile;
+        mbar_arrive_expect_tx(bar(kBarFull + st), 2 * L::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_rows(&tk, dst + c * L::kChunk, bar(kBarFull + st), p.layout, c, g, sk.chunk,
+                   kt * 128, w.bat);
+          tma_rows(&tv, dst + L::kTile + c * L::kChunk, bar(kBarFull + st), p.layout, c, g,
+                   sk.chunk, kt * 128, w.bat);
+        }
+        if (st) ++nf1; else ++nf0;
+        return true;
+      });
+      if (!ok) {
+        record_failure(p, abort_flag);
+        bounded_wait(bar(kBarFix), 0, kDrainNs, nullptr);
+        if (nf0) bounded_wait(bar(kBarFull), (nf0 - 1) & 1, kDrainNs, nullptr);
+        if (nf1) bounded_wait(bar(kBarFull + 1), (nf1 - 1) & 1, kDrainNs, nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ;
+    const uint64_t dQ = smem_desc_sw128(sbase + L::kFix, 16, 1024);
+    const uint64_t dDO = smem_desc_sw128(sbase + L::kFix + L::kTile, 16, 1024);
+    uint64_t dKk[2], dVk[2], dKmn[2];
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      const uint32_t a = sbase + L::kStage + st * 2 * L::kTile;
+      dKk[st] = smem_desc_sw128(a, 16, 1024);
+      dVk[st] = smem_desc_sw128(a + L::kTile, 16, 1024);
+      dKmn[st] = smem_desc_sw128(a, L::kChunk, 1024);
+    }
+    bool ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarFix), 0, p.timeout_ns, abort_flag) &&
+                                      bounded_wait(bar(kBarFull), 0, p.timeout_ns, abort_flag));
+    if (ok) {
+      tc_fence_after_sync();
+      if (elect_one()) {
+        issue_ss<D>(tS, dQ, dKk[0]);     // S(0) = Q K^T
+        mma_commit(bar(kBarSF));
+        issue_ss<D>(tDP, dDO, dVk[0]);   // dP(0) = dO V^T
+        mma_commit(bar(kBarDPF));
+      }
+      __syncwarp();
+    }
+    for (int t = 0; t < T && ok; ++t) {
+      const int st = t & 1, st1 = (t + 1) & 1;
+      const uint32_t ph1 = static_cast<uint32_t>((t + 1) >> 1) & 1;
+      const bool has_next = t + 1 < T;
+      const uint32_t par = static_cast<uint32_t>(t) & 1;
+      if (has_next) {
+        // the workers have read S(t): S(t+1) may overwrite it
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW1), par, p.timeout_ns, abort_flag) &&
+                                     bounded_wait(bar(kBarFull + st1), ph1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) {
+          issue_ss<D>(tS, dQ, dKk[st1]);
+          mma_commit(bar(kBarSF));
+        }
+        __syncwarp();
+      }
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW2), par, p.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      if (elect_one()) {
+        issue_ts<D>(tDQ, tDP, dKmn[st], t > 0);   // dQ += dS K
+        mma_commit(bar(kBarEmpty + st));
+        if (has_next) {
+          issue_ss<D>(tDP, dDO, dVk[st1]);
+          mma_commit(bar(kBarDPF));
+        } else {
+          mma_commit(bar(kBarDone));
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      if (lane == 0) record_failure(p, abort_flag);
+      if (elect_one()) mma_commit(bar(kBarDrain));
+      __syncwarp();
+      bounded_wait(bar(kBarDrain), 0, kDrainNs, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- workers
+    const int quarter = warp & 3;      // TMEM lanes = query rows
+    const int half = warp >> 2;        // key columns [64 half, 64 half + 64)
+    const int i = w.qt * 128 + quarter * 32 + lane;
+    const bool valid = i < w.sq.len;
+    const int qpos = valid ? w.sq.base + i * w.sq.stride : -1;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + kColS + lane_off + half * 64;
+    const uint32_t tDP = tmem + kColDP + lane_off + half * 64;
+    const float* st_row = stats_tile(p, w.bat, w.h, w.sq.chunk, w.qt) + quarter * 32 + lane;
+    const float l2 = st_row[0];     // +inf past the chunk's end
+    const float drow = st_row[128];
+    const float2 cc = make_float2(p.scale_log2, p.scale_log2);
+    const float2 ml = make_float2(-l2, -l2);
+    const float2 dd = make_float2(drow, drow);
+    bool ok = true;
+    walk_ktiles<ZIG>(p, w, [&](int t, const Seg& sk, int kt) {
+      const uint32_t par = static_cast<uint32_t>(t) & 1;
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarSF), par, p.timeout_ns, abort_flag))) {
+        ok = false;
+        return false;
+      }
+      tc_fence_after_sync();
+      float a[64];
+      {
+        uint32_t r[64];
+        tmem_ld_x64(tS, r);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 x = ffma2(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cc, ml);
+          a[c] = ex2(x.x);
+          a[c + 1] = ex2(x.y);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarW1));
+      // causal / segment-tail mask: the visible keys of the tile are a prefix
+      const int cnt = seg_visible(sk, p.causal, kt * 128, 128, qpos) - half * 64;
+      if (__any_sync(0xffffffffu, cnt < 64)) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c >= cnt) a[c] = 0.f;
+      }
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarDPF), par, p.timeout_ns, abort_flag))) {
+        ok = false;
+        return false;
+      }
+      tc_fence_after_sync();
+      {
+        uint32_t r[64];
+        tmem_ld_x64(tDP, r);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 e = fmul2(make_float2(a[c], a[c + 1]),
+                                 fadd2(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])),
+                                       make_float2(-dd.x, -dd.y)));
+          pk[c >> 1] = pack_bf16x2(e.x, e.y);
+        }
+        tmem_st_x32(tDP, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarW2));
+      return true;
+    });
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarDone), 0, p.timeout_ns, abort_flag));
+    if (!ok) {
+      if (lane == 0) record_failure(p, abort_flag);
+    } else {
+      tc_fence_after_sync();
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dq) +
+                           ((static_cast<size_t>(w.bat) * p.N + (valid ? qpos : 0)) * p.H + w.h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = half * (D / 2) + c * 32;
+        uint32_t r[32];
+        tmem_ld_x32(tmem + kColDQ + lane_off + col, r);
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * p.scale, __uint_as_float(r[8 * q + 1]) * p.scale);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * p.scale, __uint_as_float(r[8 * q + 3]) * p.scale);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * p.scale, __uint_as_float(r[8 * q + 5]) * p.scale);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * p.scale, __uint_as_float(r[8 * q + 7]) * p.scale);
+            d4[q] = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Sets the dynamic shared-memory limit of a kernel once per device.
+template <typename K>
+cudaError_t set_smem_once(K kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load() & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit);
+  return e;
+}
+
+template <int D, bool ZIG>
+cudaError_t launch_dkdv_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  static std::atomic<unsigned long long> done{0};
+  const int smem = BwdSmem<D>::kAlloc;
+  cudaError_t e = set_smem_once(bwd_dkdv_kernel<D, ZIG>, smem, done);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.B) * p.G * p.X * p.nt;
+  if (grid <= 0) return cudaSuccess;
+  bwd_dkdv_kernel<D, ZIG><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tdo, tk, tv);
+  return cudaGetLastError();
+}
+
+template <int D, bool ZIG>
+cudaError_t launch_dq_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                        const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  static std::atomic<unsigned long long> done{0};
+  const int smem = BwdSmem<D>::kAlloc;
+  cudaError_t e = set_smem_once(bwd_dq_kernel<D, ZIG>, smem, done);
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(p.B) * p.H * p.X * p.nt;
+  if (grid <= 0) return cudaSuccess;
+  bwd_dq_kernel<D, ZIG><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tdo, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t st) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.X * p.nt * 128;
+  const int tpr = p.D / 8;
+  long long blocks = (rows * tpr + 255) / 256;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  if (blocks < 1) blocks = 1;
+  if (p.D == 64)
+    bwd_prep_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  else
+    bwd_prep_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  const bool zig = p.layout == kZigzag;
+  if (p.D == 64)
+    return zig ? launch_dkdv_d<64, true>(p, tq, tdo, tk, tv, st)
+               : launch_dkdv_d<64, false>(p, tq, tdo, tk, tv, st);
+  return zig ? launch_dkdv_d<128, true>(p, tq, tdo, tk, tv, st)
+             : launch_dkdv_d<128, false>(p, tq, tdo, tk, tv, st);
+}
+
+cudaError_t launch_bwd_dq(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  const bool zig = p.layout == kZigzag;
+  if (p.D == 64)
+    return zig ? launch_dq_d<64, true>(p, tq, tdo, tk, tv, st)
+               : launch_dq_d<64, false>(p, tq, tdo, tk, tv, st);
+  return zig ? launch_dq_d<128, true>(p, tq, tdo, tk, tv, st)
+             : launch_dq_d<128, false>(p, tq, tdo, tk, tv, st);
+}
+
+}  // namespace ra

@@ -40,6 +40,31 @@ struct RingParams {
   int* status;            // the device status word
 };
 
+// Everything the backward kernels need about one call. q, o, dout, dq
+// [B,N,H,d]; k, v, dk, dv [B,N,G,d]; lse [B,H,N]. Tiles are addressed by (chunk,
+// 128-row tile) as in the forward: X chunks of L rows, nt = ceil(L / 128) tiles
+// per chunk (contiguous, striped: chunk = shard; zigzag: chunk = half-shard).
+struct BwdParams {
+  int32_t B, N, H, G, D, S, P, layout, causal;
+  int32_t X, L, nt;
+  float scale;            // score scale (natural units)
+  float scale_log2;       // scale * log2(e)
+  uint64_t timeout_ns;    // limit of every device-side wait
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  // Per (batch, head, chunk, tile), 256 floats: LSE * log2(e) of the tile's 128
+  // rows, then D = rowsum(dO * O); rows past the chunk's end hold +inf and 0.
+  float* ws;
+  void* dq;
+  void* dk;
+  void* dv;
+  int* status;
+};
+
 // Launchers (return a cudaError_t of the launch).
 cudaError_t launch_ring_tc(const RingParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t st);
@@ -58,6 +83,14 @@ cudaError_t launch_decode_partials(const RingParams& p, int n_q, int q_pos0, flo
                                    float* lse_parts, cudaStream_t st);
 // Keys per chunk of a shard in the decode partial phase.
 int decode_chunk_keys(int S);
+
+// Backward: statistics pass, then the dK/dV and dQ tensor-core kernels.
+// tq, tdo: [B,N,H,d] views; tk, tv: [B,N,G,d] views (as for the forward).
+cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+cudaError_t launch_bwd_dq(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 
 // Bytes of dynamic shared memory the tensor-core kernel uses for head_dim D.
 int ring_tc_smem_bytes(int D);

@@ -112,6 +112,18 @@ def make_qkv(w: Workload, device="cpu", seed: Optional[int] = None):
     return q, k, v
 
 
+def make_dout(w: Workload, device="cpu", seed: Optional[int] = None):
+    """Upstream gradient dO [B,N,H,d] for the backward: N(0, 1) in fp32 rounded to
+    bf16, from its own generator seeded seed+2 (seed defaults to the workload's)."""
+    seed = w.seed if seed is None else seed
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed + 2)
+    x = torch.randn((w.batch, w.seqlen, w.heads, w.head_dim), generator=g, device=dev,
+                    dtype=torch.float32)
+    return x.to(torch.bfloat16)
+
+
 def make_merge_inputs(n_parts: int, batch: int, seqlen: int, heads: int, head_dim: int,
                       device="cpu", seed: int = 7, neg_inf_frac: float = 0.01):
     """Per-part normalised outputs O_p ~ N(0,1) fp32 [n,B,N,H,d] and log-sum-exps

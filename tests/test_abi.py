@@ -121,3 +121,33 @@ def test_decode_workspace_and_argument_checks(lib):
         _lib.RA_ERR_INVALID_ARG                      # query positions past the cache
     assert lib.ring_attn_decode(ctypes.byref(pr), 0, 0, *args, need, None) == \
         _lib.RA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("layout,N,P,tiles_per_bh", [
+    (0, 1000, 4, 4 * 2),        # 4 shards of 250 rows: 2 tiles each
+    (1, 1000, 4, 4 * 2),        # striped: the same per shard
+    (2, 1040, 4, 8 * 2),        # zigzag: 8 chunks of 130 rows: 2 tiles each
+    (0, 256, 1, 2),
+])
+def test_bwd_workspace_bytes(lib, layout, N, P, tiles_per_bh):
+    pr = _pr(seqlen=N, P=P, layout=layout, heads=6, kv_heads=3, batch=2)
+    assert lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr)) == 2 * 6 * tiles_per_bh * 1024
+    assert lib.ring_attn_bwd_workspace_bytes(ctypes.byref(_pr(heads=3))) == 0
+    assert lib.ring_attn_bwd_workspace_bytes(None) == 0
+
+
+def test_bwd_argument_checks(lib):
+    pr = _pr()
+    need = lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr))
+    good = [FAKE] * 9
+    assert lib.ring_attn_bwd(ctypes.byref(pr), *good, FAKE, need - 16, None) == \
+        _lib.RA_ERR_INVALID_ARG                      # workspace too small
+    for i in range(10):
+        ptrs = [FAKE] * 10
+        ptrs[i] = None
+        assert lib.ring_attn_bwd(ctypes.byref(pr), *ptrs, need, None) == _lib.RA_ERR_INVALID_ARG
+        ptrs[i] = ctypes.c_void_p(0x10004)
+        assert lib.ring_attn_bwd(ctypes.byref(pr), *ptrs, need, None) == _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_bwd(ctypes.byref(_pr(head_dim=96)), *[FAKE] * 10, need, None) == \
+        _lib.RA_ERR_UNSUPPORTED
+    assert lib.ring_attn_bwd(None, *[FAKE] * 10, need, None) == _lib.RA_ERR_INVALID_ARG
