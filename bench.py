@@ -39,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from online_softmax_merge_gb300 import replicas  # noqa: E402
-from online_softmax_merge_gb300.inputs import WORKLOAD_TEXT, WORKLOADS, make_merge_inputs, make_qkv  # noqa: E402
+from online_softmax_merge_gb300.inputs import WORKLOAD_TEXT, WORKLOADS, make_dout, make_merge_inputs, make_qkv  # noqa: E402
 
 METRIC = "ring-attn fwd TFLOP/s (causal-adj) & % GB300 BF16 tensor peak; tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -391,6 +391,33 @@ def run_ours(args, w):
                               f"P={w.P} {w.layout}); partials per (shard, 4096-key chunk) + merge"}
         del qd, ws, od, ld
 
+    # ---- backward ring on the same workload, from this forward's O and LSE
+    bwd = None
+    if not args.no_bwd:
+        do = make_dout(w, device=dev)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        need = ra.bwd_workspace_bytes(w.batch, w.seqlen, w.heads, w.kv_heads, w.head_dim, w.P,
+                                      w.layout, w.causal)
+        ws = torch.empty(need // 4, dtype=torch.float32, device=dev)
+
+        def back():
+            ra.bwd(q, k, v, o, lse, do, w.P, w.layout, w.causal, dq=gq, dk=gk, dv=gv, workspace=ws)
+
+        back()
+        torch.cuda.synchronize(dev)
+        ms = time_launches(back, max(2, min(args.steps, 3)), stream)
+        if ra.last_error(dev) != 0:
+            raise RuntimeError("device-side wait timed out in the backward")
+        bflops = 2.5 * flops_step            # five matrix products of the forward's size
+        tf = bflops / (statistics.mean(ms) * 1e-3) / 1e12
+        bwd = {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+               "frac": tf / peak_tf, "ms": statistics.mean(ms), "algorithmic_flops": bflops,
+               "launches_per_call": 3,
+               "kernels": ["bwd_prep_kernel", "bwd_dkdv_kernel<128>", "bwd_dq_kernel<128>"],
+               "workload": f"dQ, dK, dV of the {w.name} forward for a N(0,1) bf16 upstream "
+                           f"gradient; FLOPs = 2.5 x the forward's causal-adjusted FLOPs"}
+        del do, gq, gk, gv, ws
+
     # ---- the oracle on the host cores (rank 0 only)
     cpu = None
     if info.is_main and not args.no_cpu_baseline:
@@ -414,6 +441,7 @@ def run_ours(args, w):
                          "kernel": "ring_tc_kernel<128>", "launch_ms": statistics.mean(launch_ms)},
             "merge_roofline": merge,
             "decode_roofline": decode,
+            "bwd_roofline": bwd,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -438,6 +466,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-merge", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
