@@ -21,7 +21,10 @@
 //    shard in the reverse ring order u = (b - s) mod P, skipping tiles the causal
 //    mask leaves empty. dK and dV stay in TMEM for the whole walk;
 //  * bwd_dq: a CTA owns one 128-row query tile of one head and walks the key
-//    tiles of blocks b = (u + s) mod P; dQ stays in TMEM.
+//    tiles of blocks b = (u + s) mod P; dQ stays in TMEM, and so do the tile's
+//    Q and dO (the workers store their rows there once), so all three products
+//    of this kernel read only K or V from shared memory, streamed through three
+//    stages.
 // Both tensor-core kernels have 10 warps: warp 9 streams two tiles per step
 // through two shared-memory stages with TMA, warp 8 issues the tcgen05 MMAs
 // (one elected lane of a warp-uniform loop), and warps 0-7 are the element-wise
@@ -35,8 +38,9 @@
 // dP^T [384,512)):  MMA order  dP^T(t) | dV += A^T(t) dO(t) | S^T(t+1) |
 // dK += dS^T(t) Q(t) | dP^T(t+1) ...  so the workers' phase 1 overlaps dP^T(t)
 // and phase 2 overlaps dV(t) and S^T(t+1).
-// dQ kernel, per key tile t (TMEM: S [0,128), dP [128,256), dQ [256,256+D)):
-// MMA order  dP(t) | S(t+1) | dQ += dS(t) K(t) | dP(t+1) ...
+// dQ kernel, per key tile t (TMEM: S [0,128), dP [128,256), dQ [256,256+D),
+// Q and dO as bf16 pairs [384,512)): MMA order  dP(t) | S(t+1) | dQ += dS(t) K(t)
+// | dP(t+1) ...
 // The tensor core runs these in issue order, so an MMA that overwrites a TMEM
 // region is always behind the MMAs that read it; the workers signal when they
 // have read a region into registers.
@@ -71,6 +75,18 @@ struct BwdSmem {
   static constexpr int kBar = kStats + 2 * kStatBytes;
   static constexpr int kBytes = kBar + 256;
   // One CTA per SM: it owns all 512 TMEM columns.
+  static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+// dQ kernel: K/V stages only (Q and dO live in TMEM).
+template <int D>
+struct DqSmem {
+  static constexpr int kChunk = 128 * 128;
+  static constexpr int kTile = (D / 64) * kChunk;
+  static constexpr int kStages = 3;
+  static constexpr int kStage = 0;                  // stage st: K at kStage + 2 st kTile, V after
+  static constexpr int kBar = kStages * 2 * kTile;
+  static constexpr int kBytes = kBar + 256;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
@@ -129,6 +145,20 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint6
     mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8,
            b_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
            (kk > 0 || accumulate) ? 1u : 0u);
+}
+
+// D[tmem] = A B^T with A [128 x D] bf16 in TMEM (two elements per column, the
+// k-th 16-element slice at a_tmem + 8 k) and B a [128 x D] K-major tile in
+// shared memory: D/16 MMAs of 128 x 128 x 16.
+template <int D>
+__device__ __forceinline__ void issue_ts_kmajor(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off =
+        static_cast<uint64_t>(((kk >> 2) * BwdSmem<D>::kChunk + (kk & 3) * 32) >> 4);
+    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+  }
 }
 
 __device__ __forceinline__ int ring_mod(int x, int P) {
@@ -369,23 +399,19 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     const uint32_t tS = tmem + kColS, tDP = tmem + kColDP;
     const uint64_t dK = smem_desc_sw128(sbase + L::kFix, 16, 1024);
     const uint64_t dV = smem_desc_sw128(sbase + L::kFix + L::kTile, 16, 1024);
-    uint64_t dQk[2], dDOk[2], dQmn[2], dDOmn[2];
-#pragma unroll
-    for (int st = 0; st < 2; ++st) {
-      const uint32_t a = sbase + L::kStage + st * 2 * L::kTile;
-      dQk[st] = smem_desc_sw128(a, 16, 1024);
-      dDOk[st] = smem_desc_sw128(a + L::kTile, 16, 1024);
-      dQmn[st] = smem_desc_sw128(a, L::kChunk, 1024);
-      dDOmn[st] = smem_desc_sw128(a + L::kTile, L::kChunk, 1024);
-    }
+    // Q (which = 0) or dO (which = 1) of stage st, K-major or MN-major
+    auto sdesc = [&](int st, int which, bool mn) -> uint64_t {
+      return smem_desc_sw128(sbase + L::kStage + st * 2 * L::kTile + which * L::kTile,
+                             mn ? L::kChunk : 16, 1024);
+    };
     bool ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarFix), 0, p.timeout_ns, abort_flag) &&
                                       bounded_wait(bar(kBarFull), 0, p.timeout_ns, abort_flag));
     if (ok) {
       tc_fence_after_sync();
       if (elect_one()) {
-        issue_ss<D>(tS, dK, dQk[0]);     // S^T(0) = K Q^T
+        issue_ss<D>(tS, dK, sdesc(0, 0, false));     // S^T(0) = K Q^T
         mma_commit(bar(kBarSF));
-        issue_ss<D>(tDP, dV, dDOk[0]);   // dP^T(0) = V dO^T
+        issue_ss<D>(tDP, dV, sdesc(0, 1, false));    // dP^T(0) = V dO^T
         mma_commit(bar(kBarDPF));
       }
       __syncwarp();
@@ -400,7 +426,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         break;
       }
       tc_fence_after_sync();
-      if (elect_one()) issue_ts<D>(tDV, tS, dDOmn[st], t > 0);   // dV += A^T dO
+      if (elect_one()) issue_ts<D>(tDV, tS, sdesc(st, 1, true), t > 0);   // dV += A^T dO
       __syncwarp();
       if (has_next) {
         if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarFull + st1), ph1, p.timeout_ns, abort_flag))) {
@@ -409,7 +435,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         }
         tc_fence_after_sync();
         if (elect_one()) {
-          issue_ss<D>(tS, dK, dQk[st1]);
+          issue_ss<D>(tS, dK, sdesc(st1, 0, false));
           mma_commit(bar(kBarSF));
         }
         __syncwarp();
@@ -420,10 +446,10 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       }
       tc_fence_after_sync();
       if (elect_one()) {
-        issue_ts<D>(tDK, tDP, dQmn[st], t > 0);                    // dK += dS^T Q
+        issue_ts<D>(tDK, tDP, sdesc(st, 0, true), t > 0);          // dK += dS^T Q
         mma_commit(bar(kBarEmpty + st));
         if (has_next) {
-          issue_ss<D>(tDP, dV, dDOk[st1]);
+          issue_ss<D>(tDP, dV, sdesc(st1, 1, false));
           mma_commit(bar(kBarDPF));
         } else {
           mma_commit(bar(kBarDone));
@@ -637,13 +663,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
               const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv) {
-  using L = BwdSmem<D>;
+  using L = DqSmem<D>;
+  constexpr int NS = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kNumBars + 4);
+  // barriers: kBarFix, then NS full, NS empty, and the per-step ones after them
+  constexpr int kFull = 1, kEmpty = 1 + NS, kSF = 1 + 2 * NS, kDPF = kSF + 1, kW1 = kSF + 2,
+                kW2 = kSF + 3, kDone = kSF + 4, kDrain = kSF + 5, kBars = kSF + 6;
+  static_assert(8 * kBars + 8 <= 256, "barrier area");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kBars + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
 
   const int warp = threadIdx.x >> 5;
@@ -668,9 +699,10 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
-    mbar_init(bar(kBarW1), kWorkers);
-    mbar_init(bar(kBarW2), kWorkers);
+    for (int i = 0; i < kBars; ++i) mbar_init(bar(i), 1);
+    mbar_init(bar(kBarFix), kWorkers);   // the workers put Q and dO into TMEM
+    mbar_init(bar(kW1), kWorkers);
+    mbar_init(bar(kW2), kWorkers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -679,8 +711,6 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
     tmem_relinquish();
   }
   if (warp == kTmaWarp && lane == 0) {
-    prefetch_tensormap(&tq);
-    prefetch_tensormap(&tdo);
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
   }
@@ -688,115 +718,108 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  // TMEM: S, dP (fp32), dQ (fp32), and the stationary Q and dO tiles as bf16
+  // pairs, the A operands of S = Q K^T and dP = dO V^T.
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 384, kColDO = 384 + D / 2;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      uint32_t nf0 = 0, nf1 = 0;
+      uint32_t nf[NS] = {};   // loads issued per stage (for the drain on abort)
       bool ok = true;
-      mbar_arrive_expect_tx(bar(kBarFix), 2 * L::kTile);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_rows(&tq, sbase + L::kFix + c * L::kChunk, bar(kBarFix), p.layout, c, w.h,
-                 w.sq.chunk, w.qt * 128, w.bat);
-        tma_rows(&tdo, sbase + L::kFix + L::kTile + c * L::kChunk, bar(kBarFix), p.layout, c, w.h,
-                 w.sq.chunk, w.qt * 128, w.bat);
-      }
       const int g = (w.h * p.G) / p.H;
       walk_ktiles<ZIG>(p, w, [&](int t, const Seg& sk, int kt) {
-        const int st = t & 1;
-        const uint32_t n = static_cast<uint32_t>(t >> 1);
-        if (t >= 2 && !bounded_wait(bar(kBarEmpty + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+        const int st = t % NS;
+        const uint32_t n = static_cast<uint32_t>(t / NS);
+        if (t >= NS && !bounded_wait(bar(kEmpty + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           return false;
         }
         const uint32_t dst = sbase + L::kStage + st * 2 * L::kTile;
-        mbar_arrive_expect_tx(bar(kBarFull + st), 2 * L::kTile);
+        mbar_arrive_expect_tx(bar(kFull + st), 2 * L::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          tma_rows(&tk, dst + c * L::kChunk, bar(kBarFull + st), p.layout, c, g, sk.chunk,
+          tma_rows(&tk, dst + c * L::kChunk, bar(kFull + st), p.layout, c, g, sk.chunk,
                    kt * 128, w.bat);
-          tma_rows(&tv, dst + L::kTile + c * L::kChunk, bar(kBarFull + st), p.layout, c, g,
+          tma_rows(&tv, dst + L::kTile + c * L::kChunk, bar(kFull + st), p.layout, c, g,
                    sk.chunk, kt * 128, w.bat);
         }
-        if (st) ++nf1; else ++nf0;
+#pragma unroll
+        for (int x = 0; x < NS; ++x) nf[x] += (x == st);
         return true;
       });
       if (!ok) {
         record_failure(p, abort_flag);
-        bounded_wait(bar(kBarFix), 0, kDrainNs, nullptr);
-        if (nf0) bounded_wait(bar(kBarFull), (nf0 - 1) & 1, kDrainNs, nullptr);
-        if (nf1) bounded_wait(bar(kBarFull + 1), (nf1 - 1) & 1, kDrainNs, nullptr);
+#pragma unroll
+        for (int x = 0; x < NS; ++x)
+          if (nf[x]) bounded_wait(bar(kFull + x), (nf[x] - 1) & 1, kDrainNs, nullptr);
       }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
     const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColDQ;
-    const uint64_t dQ = smem_desc_sw128(sbase + L::kFix, 16, 1024);
-    const uint64_t dDO = smem_desc_sw128(sbase + L::kFix + L::kTile, 16, 1024);
-    uint64_t dKk[2], dVk[2], dKmn[2];
-#pragma unroll
-    for (int st = 0; st < 2; ++st) {
-      const uint32_t a = sbase + L::kStage + st * 2 * L::kTile;
-      dKk[st] = smem_desc_sw128(a, 16, 1024);
-      dVk[st] = smem_desc_sw128(a + L::kTile, 16, 1024);
-      dKmn[st] = smem_desc_sw128(a, L::kChunk, 1024);
-    }
+    const uint32_t tQ = tmem + kColQ, tDO = tmem + kColDO;
+    // K (K-major for S, MN-major for dQ) and V (K-major) of stage st
+    auto kdesc = [&](int st, bool mn) -> uint64_t {
+      return smem_desc_sw128(sbase + L::kStage + st * 2 * L::kTile, mn ? L::kChunk : 16, 1024);
+    };
+    auto vdesc = [&](int st) -> uint64_t {
+      return smem_desc_sw128(sbase + L::kStage + st * 2 * L::kTile + L::kTile, 16, 1024);
+    };
     bool ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarFix), 0, p.timeout_ns, abort_flag) &&
-                                      bounded_wait(bar(kBarFull), 0, p.timeout_ns, abort_flag));
+                                      bounded_wait(bar(kFull), 0, p.timeout_ns, abort_flag));
     if (ok) {
       tc_fence_after_sync();
       if (elect_one()) {
-        issue_ss<D>(tS, dQ, dKk[0]);     // S(0) = Q K^T
-        mma_commit(bar(kBarSF));
-        issue_ss<D>(tDP, dDO, dVk[0]);   // dP(0) = dO V^T
-        mma_commit(bar(kBarDPF));
+        issue_ts_kmajor<D>(tS, tQ, kdesc(0, false));    // S(0) = Q K^T
+        mma_commit(bar(kSF));
+        issue_ts_kmajor<D>(tDP, tDO, vdesc(0));        // dP(0) = dO V^T
+        mma_commit(bar(kDPF));
       }
       __syncwarp();
     }
     for (int t = 0; t < T && ok; ++t) {
-      const int st = t & 1, st1 = (t + 1) & 1;
-      const uint32_t ph1 = static_cast<uint32_t>((t + 1) >> 1) & 1;
+      const int st = t % NS, st1 = (t + 1) % NS;
+      const uint32_t ph1 = static_cast<uint32_t>((t + 1) / NS) & 1;
       const bool has_next = t + 1 < T;
       const uint32_t par = static_cast<uint32_t>(t) & 1;
       if (has_next) {
         // the workers have read S(t): S(t+1) may overwrite it
-        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW1), par, p.timeout_ns, abort_flag) &&
-                                     bounded_wait(bar(kBarFull + st1), ph1, p.timeout_ns, abort_flag))) {
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kW1), par, p.timeout_ns, abort_flag) &&
+                                     bounded_wait(bar(kFull + st1), ph1, p.timeout_ns, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         if (elect_one()) {
-          issue_ss<D>(tS, dQ, dKk[st1]);
-          mma_commit(bar(kBarSF));
+          issue_ts_kmajor<D>(tS, tQ, kdesc(st1, false));
+          mma_commit(bar(kSF));
         }
         __syncwarp();
       }
-      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW2), par, p.timeout_ns, abort_flag))) {
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kW2), par, p.timeout_ns, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       if (elect_one()) {
-        issue_ts<D>(tDQ, tDP, dKmn[st], t > 0);   // dQ += dS K
-        mma_commit(bar(kBarEmpty + st));
+        issue_ts<D>(tDQ, tDP, kdesc(st, true), t > 0);   // dQ += dS K
+        mma_commit(bar(kEmpty + st));
         if (has_next) {
-          issue_ss<D>(tDP, dDO, dVk[st1]);
-          mma_commit(bar(kBarDPF));
+          issue_ts_kmajor<D>(tDP, tDO, vdesc(st1));
+          mma_commit(bar(kDPF));
         } else {
-          mma_commit(bar(kBarDone));
+          mma_commit(bar(kDone));
         }
       }
       __syncwarp();
     }
     if (!ok) {
       if (lane == 0) record_failure(p, abort_flag);
-      if (elect_one()) mma_commit(bar(kBarDrain));
+      if (elect_one()) mma_commit(bar(kDrain));
       __syncwarp();
-      bounded_wait(bar(kBarDrain), 0, kDrainNs, nullptr);
+      bounded_wait(bar(kDrain), 0, kDrainNs, nullptr);
     }
     __syncwarp();
   } else {
@@ -815,10 +838,35 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
     const float2 cc = make_float2(p.scale_log2, p.scale_log2);
     const float2 ml = make_float2(-l2, -l2);
     const float2 dd = make_float2(drow, drow);
+    {
+      // Half 0 stores this row of Q, half 1 this row of dO, into TMEM as bf16
+      // pairs (the memory order of the row); rows past the chunk's end are 0.
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(half == 0 ? p.q : p.dout) +
+          ((static_cast<size_t>(w.bat) * p.N + (valid ? qpos : 0)) * p.H + w.h) * D);
+      const uint32_t dst = tmem + (half == 0 ? kColQ : kColDO) + lane_off;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = valid ? src[c * 8 + j] : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * j] = x.x;
+          r[4 * j + 1] = x.y;
+          r[4 * j + 2] = x.z;
+          r[4 * j + 3] = x.w;
+        }
+        tmem_st_x32(dst + c * 32, r);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarFix));
+    }
     bool ok = true;
     walk_ktiles<ZIG>(p, w, [&](int t, const Seg& sk, int kt) {
       const uint32_t par = static_cast<uint32_t>(t) & 1;
-      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarSF), par, p.timeout_ns, abort_flag))) {
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kSF), par, p.timeout_ns, abort_flag))) {
         ok = false;
         return false;
       }
@@ -836,7 +884,7 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarW1));
+      if (lane == 0) mbar_arrive(bar(kW1));
       // causal / segment-tail mask: the visible keys of the tile are a prefix
       const int cnt = seg_visible(sk, p.causal, kt * 128, 128, qpos) - half * 64;
       if (__any_sync(0xffffffffu, cnt < 64)) {
@@ -844,7 +892,7 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
         for (int c = 0; c < 64; ++c)
           if (c >= cnt) a[c] = 0.f;
       }
-      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarDPF), par, p.timeout_ns, abort_flag))) {
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kDPF), par, p.timeout_ns, abort_flag))) {
         ok = false;
         return false;
       }
@@ -865,10 +913,10 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarW2));
+      if (lane == 0) mbar_arrive(bar(kW2));
       return true;
     });
-    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarDone), 0, p.timeout_ns, abort_flag));
+    if (ok) ok = __all_sync(0xffffffffu, bounded_wait(bar(kDone), 0, p.timeout_ns, abort_flag));
     if (!ok) {
       if (lane == 0) record_failure(p, abort_flag);
     } else {
@@ -934,7 +982,7 @@ template <int D, bool ZIG>
 cudaError_t launch_dq_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                         const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
   static std::atomic<unsigned long long> done{0};
-  const int smem = BwdSmem<D>::kAlloc;
+  const int smem = DqSmem<D>::kAlloc;
   cudaError_t e = set_smem_once(bwd_dq_kernel<D, ZIG>, smem, done);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.B) * p.H * p.X * p.nt;
