@@ -215,7 +215,8 @@ ra_status ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const
                         void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace ring_attn_bwd needs for this problem (0 if the problem is
- * invalid): 1 KiB per 128-row query tile of every (batch, head). Pure host code. */
+ * invalid): 9 KiB per 128-row query tile of every (batch, head) plus 4 KiB. Pure
+ * host code. */
 size_t ring_attn_bwd_workspace_bytes(const ra_problem* p);
 
 /* Shard ownership on the HOST: owner[t], local[t] for t < N and

@@ -213,13 +213,29 @@ size_t decode_workspace(const ra_problem* pr, int32_t n_q) {
   return parts * rows * (static_cast<size_t>(pr->head_dim) + 1) * sizeof(float);
 }
 
-// Backward statistics workspace: 256 floats per (batch, head, chunk, 128-row tile).
-size_t bwd_workspace(const ra_problem* pr) {
+// Backward workspace, per (batch, head, chunk, 128-row query tile): 1 KiB of
+// statistics plus two 4 KiB extension tiles; then one 4 KiB key-side tile.
+int64_t bwd_tiles(const ra_problem* pr) {
   const int S = pr->seqlen / pr->P;
   const int X = pr->layout == RA_LAYOUT_ZIGZAG ? 2 * pr->P : pr->P;
   const int L = pr->layout == RA_LAYOUT_ZIGZAG ? S / 2 : S;
-  const size_t nt = static_cast<size_t>((L + 127) / 128);
-  return static_cast<size_t>(pr->batch) * pr->heads * X * nt * 256 * sizeof(float);
+  return static_cast<int64_t>(pr->batch) * pr->heads * X * ((L + 127) / 128);
+}
+size_t bwd_workspace(const ra_problem* pr) {
+  return static_cast<size_t>(bwd_tiles(pr)) * (1024 + 2 * 4096) + 4096;
+}
+
+// 2-D map over the extension rows (16 bf16 each), boxes of 128 rows, 32-byte swizzle.
+bool encode_ext(CUtensorMap* m, const void* base, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {16, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {32};
+  const cuuint32_t box[2] = {16, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -401,6 +417,8 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
   for (const void* ptr : in)
     if (ptr == nullptr || !aligned16(ptr)) return RA_ERR_INVALID_ARG;
   if (workspace_bytes < bwd_workspace(pr)) return RA_ERR_INVALID_ARG;
+  // the extension rows are addressed by 32-bit TMA coordinates
+  if (bwd_tiles(pr) * 2 * 128 + 128 >= (static_cast<int64_t>(1) << 31)) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
   RingParams f;
@@ -419,6 +437,7 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
   p.X = f.X;
   p.L = f.L;
   p.nt = f.nq;
+  p.tiles = static_cast<int32_t>(bwd_tiles(pr));
   p.scale = f.scale;
   p.scale_log2 = f.scale_log2;
   p.timeout_ns = f.timeout_ns;
@@ -436,14 +455,16 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // zigzag tiles by chunk: the contiguous view with X = 2P chunks of L = S/2 tokens
   const int ml = p.layout == kZigzag ? kContiguous : p.layout;
-  CUtensorMap tq, tdo, tk, tv;
+  CUtensorMap tq, tdo, tk, tv, text;
+  const void* ext = static_cast<const uint8_t*>(workspace) + static_cast<size_t>(p.tiles) * 1024;
   if (!encode_rows(&tq, q, p.B, p.N, p.H, p.D, p.L, p.X, ml) ||
       !encode_rows(&tdo, dout, p.B, p.N, p.H, p.D, p.L, p.X, ml) ||
       !encode_rows(&tk, k, p.B, p.N, p.G, p.D, p.L, p.X, ml) ||
-      !encode_rows(&tv, v, p.B, p.N, p.G, p.D, p.L, p.X, ml))
+      !encode_rows(&tv, v, p.B, p.N, p.G, p.D, p.L, p.X, ml) ||
+      !encode_ext(&text, ext, static_cast<int64_t>(p.tiles) * 2 * 128 + 128))
     return RA_ERR_CUDA;
   if ((st = launch_result(launch_bwd_prep(p, s))) != RA_OK) return st;
-  if ((st = launch_result(launch_bwd_dkdv(p, tq, tdo, tk, tv, s))) != RA_OK) return st;
+  if ((st = launch_result(launch_bwd_dkdv(p, tq, tdo, tk, tv, text, s))) != RA_OK) return st;
   return launch_result(launch_bwd_dq(p, tq, tdo, tk, tv, s));
 }
 

@@ -15,7 +15,8 @@
 //
 // How, on one GB300 SM. Three launches:
 //  * bwd_prep: D and LSE * log2(e) of every query row, written per 128-row tile
-//    (1 KiB each) so that a kernel fetches a tile's statistics in one bulk copy;
+//    (1 KiB each, for the dQ kernel), and the same two numbers as extension tiles
+//    for the dK/dV kernel's products (below);
 //  * bwd_dkdv: a CTA owns one 128-key tile of one kv head — the circulating
 //    block — and meets the query tiles of every query head of its group, shard by
 //    shard in the reverse ring order u = (b - s) mod P, skipping tiles the causal
@@ -37,7 +38,12 @@
 // dK/dV kernel, per query tile t (TMEM: dK [0,D), dV [D,2D), S^T [256,384),
 // dP^T [384,512)):  MMA order  dP^T(t) | dV += A^T(t) dO(t) | S^T(t+1) |
 // dK += dS^T(t) Q(t) | dP^T(t+1) ...  so the workers' phase 1 overlaps dP^T(t)
-// and phase 2 overlaps dV(t) and S^T(t+1).
+// and phase 2 overlaps dV(t) and S^T(t+1). Each query column's LSE and D enter
+// these products as one more 16-wide K slice: the key side holds ones in its
+// first three columns, the query side the bf16 split hi + mid + lo of -LSE/scale
+// (for S^T) or of -D (for dP^T), so the tensor core returns S^T - LSE/scale and
+// dP^T - D in fp32 (three bf16 terms carry ~24 significant bits) and the workers
+// need no per-column statistics.
 // dQ kernel, per key tile t (TMEM: S [0,128), dP [128,256), dQ [256,256+D),
 // Q and dO as bf16 pairs [384,512)): MMA order  dP(t) | S(t+1) | dQ += dS(t) K(t)
 // | dP(t+1) ...
@@ -63,7 +69,7 @@ constexpr int kWorkers = 8;                   // element-wise warps
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s to let in-flight copies land on abort
-constexpr int kStatBytes = 1024;              // one tile's statistics: 128 x (LSE*log2e, D)
+constexpr int kExtBytes = 128 * 16 * 2;       // one extension tile: 128 rows x 16 bf16
 
 template <int D>
 struct BwdSmem {
@@ -71,8 +77,9 @@ struct BwdSmem {
   static constexpr int kTile = (D / 64) * kChunk;   // one [128 x D] bf16 tile
   static constexpr int kFix = 0;                    // two stationary tiles
   static constexpr int kStage = 2 * kTile;          // two stages of two streamed tiles
-  static constexpr int kStats = 6 * kTile;          // dK/dV kernel: statistics, two stages
-  static constexpr int kBar = kStats + 2 * kStatBytes;
+  static constexpr int kAext = 6 * kTile;           // dK/dV kernel: key-side extension (ones)
+  static constexpr int kExt = kAext + kExtBytes;    // + stage: query-side extensions of Q, dO
+  static constexpr int kBar = kExt + 2 * 2 * kExtBytes;
   static constexpr int kBytes = kBar + 256;
   // One CTA per SM: it owns all 512 TMEM columns.
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -117,6 +124,29 @@ __device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, u
     tma_load_5d(dst, map, bar, dchunk * 64, head, chunk, i0, bat);
   else
     tma_load_5d(dst, map, bar, dchunk * 64, head, i0, chunk, bat);
+}
+
+// 2-D tiled TMA load (the extension tiles: 16 bf16 x 128 rows, 32-byte swizzle).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :
+      : "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand whose rows are 32 bytes (one
+// 16-element K slice) with the 32-byte swizzle: 8-row groups 256 bytes apart,
+// layout code 6 in bits [61,64), descriptor version 1 at bit 46.
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;            // leading offset (unused at this width)
+  d |= static_cast<uint64_t>(256 >> 4) << 32;     // stride between 8-row groups
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(6) << 61;
+  return d;
 }
 
 // D[tmem] = A B^T for two 128 x D tiles in shared memory (K-major, 128-byte
@@ -219,11 +249,42 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
     if (in && sub == 0) {
-      float* dst = p.ws + ((((static_cast<size_t>(bat) * p.H + h) * p.X + c) * p.nt + (ii >> 7)) << 8) +
-                   (ii & 127);
+      const size_t tile = ((static_cast<size_t>(bat) * p.H + h) * p.X + c) * p.nt + (ii >> 7);
+      float* dst = p.ws + (tile << 8) + (ii & 127);
       dst[0] = l2;
       dst[128] = dsum;
+      // extension rows: [-beta_hi, -beta_mid, -beta_lo, 0 ...] with beta = LSE / scale
+      // (a huge finite value for rows that contribute nothing) and the same for D
+      const float beta = (l2 == INFINITY) ? 1e30f : l2 / p.scale_log2;
+      __nv_bfloat16* ext = reinterpret_cast<__nv_bfloat16*>(p.ws + (static_cast<size_t>(p.tiles) << 8));
+      uint4* eq = reinterpret_cast<uint4*>(ext + ((tile << 7) + (ii & 127)) * 16);
+      uint4* ed = reinterpret_cast<uint4*>(ext + (((static_cast<size_t>(p.tiles) + tile) << 7) + (ii & 127)) * 16);
+      auto split3 = [](float x, uint32_t& w0, uint32_t& w1) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        const float r1 = x - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+        w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+             (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+        w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+      };
+      uint32_t a0, a1, b0, b1;
+      split3(-beta, a0, a1);
+      split3(-dsum, b0, b1);
+      eq[0] = make_uint4(a0, a1, 0u, 0u);
+      eq[1] = make_uint4(0u, 0u, 0u, 0u);
+      ed[0] = make_uint4(b0, b1, 0u, 0u);
+      ed[1] = make_uint4(0u, 0u, 0u, 0u);
     }
+  }
+  // key-side extension tile: ones in columns 0-2 of all 128 rows
+  if (blockIdx.x == 0 && threadIdx.x < 128) {
+    const uint32_t one2 = 0x3F803F80u;   // two bf16 ones
+    __nv_bfloat16* ext = reinterpret_cast<__nv_bfloat16*>(p.ws + (static_cast<size_t>(p.tiles) << 8));
+    uint4* ea = reinterpret_cast<uint4*>(ext + ((2 * static_cast<size_t>(p.tiles)) << 7) * 16 +
+                                         threadIdx.x * 16);
+    ea[0] = make_uint4(one2, 0x3F80u, 0u, 0u);
+    ea[1] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -295,7 +356,7 @@ template <int D, bool ZIG>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
                 const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tv) {
+                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap text) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -344,6 +405,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     prefetch_tensormap(&tdo);
     prefetch_tensormap(&tk);
     prefetch_tensormap(&tv);
+    prefetch_tensormap(&text);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -356,7 +418,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     if (lane == 0) {
       uint32_t nf0 = 0, nf1 = 0;   // loads issued per stage (for the drain on abort)
       bool ok = true;
-      mbar_arrive_expect_tx(bar(kBarFix), 2 * L::kTile);
+      mbar_arrive_expect_tx(bar(kBarFix), 2 * L::kTile + kExtBytes);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         tma_rows(&tk, sbase + L::kFix + c * L::kChunk, bar(kBarFix), p.layout, c, w.g,
@@ -364,6 +426,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         tma_rows(&tv, sbase + L::kFix + L::kTile + c * L::kChunk, bar(kBarFix), p.layout, c, w.g,
                  w.sk.chunk, w.kt * 128, w.bat);
       }
+      tma_load_2d(sbase + L::kAext, &text, bar(kBarFix), 0, 2 * p.tiles * 128);
       walk_qtiles<ZIG>(p, w, [&](int t, int h, const Seg& sq, int qt) {
         const int st = t & 1;
         const uint32_t n = static_cast<uint32_t>(t >> 1);
@@ -372,7 +435,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
           return false;
         }
         const uint32_t dst = sbase + L::kStage + st * 2 * L::kTile;
-        mbar_arrive_expect_tx(bar(kBarFull + st), 2 * L::kTile + kStatBytes);
+        mbar_arrive_expect_tx(bar(kBarFull + st), 2 * L::kTile + 2 * kExtBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           tma_rows(&tq, dst + c * L::kChunk, bar(kBarFull + st), p.layout, c, h, sq.chunk,
@@ -380,8 +443,10 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
           tma_rows(&tdo, dst + L::kTile + c * L::kChunk, bar(kBarFull + st), p.layout, c, h,
                    sq.chunk, qt * 128, w.bat);
         }
-        bulk_load(sbase + L::kStats + st * kStatBytes, stats_tile(p, w.bat, h, sq.chunk, qt),
-                  kStatBytes, bar(kBarFull + st));
+        const int tile = ((w.bat * p.H + h) * p.X + sq.chunk) * p.nt + qt;
+        const uint32_t ext = sbase + L::kExt + st * 2 * kExtBytes;
+        tma_load_2d(ext, &text, bar(kBarFull + st), 0, tile * 128);
+        tma_load_2d(ext + kExtBytes, &text, bar(kBarFull + st), 0, (p.tiles + tile) * 128);
         if (st) ++nf1; else ++nf0;
         return true;
       });
@@ -404,14 +469,23 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       return smem_desc_sw128(sbase + L::kStage + st * 2 * L::kTile + which * L::kTile,
                              mn ? L::kChunk : 16, 1024);
     };
+    // S^T (which = 0) or dP^T (which = 1) of stage st, with its extension slice
+    const uint64_t dA = smem_desc_sw32(sbase + L::kAext);
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, false);
+    auto products = [&](int st, int which) {
+      const uint32_t d_tmem = which == 0 ? tmem + kColS : tmem + kColDP;
+      issue_ss<D>(d_tmem, which == 0 ? dK : dV, sdesc(st, which, false));
+      mma_ss(d_tmem, dA, smem_desc_sw32(sbase + L::kExt + st * 2 * kExtBytes + which * kExtBytes),
+             kIdesc, 1u);
+    };
     bool ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarFix), 0, p.timeout_ns, abort_flag) &&
                                       bounded_wait(bar(kBarFull), 0, p.timeout_ns, abort_flag));
     if (ok) {
       tc_fence_after_sync();
       if (elect_one()) {
-        issue_ss<D>(tS, dK, sdesc(0, 0, false));     // S^T(0) = K Q^T
+        products(0, 0);     // S^T(0) = K Q^T - LSE/scale
         mma_commit(bar(kBarSF));
-        issue_ss<D>(tDP, dV, sdesc(0, 1, false));    // dP^T(0) = V dO^T
+        products(0, 1);     // dP^T(0) = V dO^T - D
         mma_commit(bar(kBarDPF));
       }
       __syncwarp();
@@ -435,7 +509,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         }
         tc_fence_after_sync();
         if (elect_one()) {
-          issue_ss<D>(tS, dK, sdesc(st1, 0, false));
+          products(st1, 0);
           mma_commit(bar(kBarSF));
         }
         __syncwarp();
@@ -449,7 +523,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         issue_ts<D>(tDK, tDP, sdesc(st, 0, true), t > 0);          // dK += dS^T Q
         mma_commit(bar(kBarEmpty + st));
         if (has_next) {
-          issue_ss<D>(tDP, dV, sdesc(st1, 1, false));
+          products(st1, 1);
           mma_commit(bar(kBarDPF));
         } else {
           mma_commit(bar(kBarDone));
@@ -474,18 +548,13 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + kColS + lane_off + half * 64;
     const uint32_t tDP = tmem + kColDP + lane_off + half * 64;
-    const float* stats = reinterpret_cast<const float*>(smem + L::kStats);
     const float2 cc = make_float2(p.scale_log2, p.scale_log2);
     bool ok = true;
     walk_qtiles<ZIG>(p, w, [&](int t, int, const Seg& sq, int qt) {
       const uint32_t par = static_cast<uint32_t>(t) & 1;
-      const float* sl = stats + (t & 1) * 256 + half * 64;   // LSE*log2e; D at +128
-      // phase 1: A^T = exp2(S^T * scale * log2e - LSE * log2e), masked. The
-      // statistics came with the stage's TMA loads: observe that barrier too.
-      if (!__all_sync(0xffffffffu,
-                      bounded_wait(bar(kBarFull + (t & 1)), static_cast<uint32_t>(t >> 1) & 1,
-                                   p.timeout_ns, abort_flag) &&
-                          bounded_wait(bar(kBarSF), par, p.timeout_ns, abort_flag))) {
+      // phase 1: A^T = exp2((S^T - LSE/scale) * scale * log2e), masked; the
+      // products already subtracted LSE/scale
+      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarSF), par, p.timeout_ns, abort_flag))) {
         ok = false;
         return false;
       }
@@ -495,20 +564,14 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         uint32_t r[64];
         tmem_ld_x64(tS, r);
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(sl + c);
-          const float2 x0 = ffma2(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cc,
-                                  make_float2(-l4.x, -l4.y));
-          const float2 x1 = ffma2(make_float2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
-                                  cc, make_float2(-l4.z, -l4.w));
-          a[c] = ex2(x0.x);
-          a[c + 1] = ex2(x0.y);
-          a[c + 2] = ex2(x1.x);
-          a[c + 3] = ex2(x1.y);
+        for (int c = 0; c < 64; c += 2) {
+          const float2 x = fmul2(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cc);
+          a[c] = ex2(x.x);
+          a[c + 1] = ex2(x.y);
         }
       }
       // Causal mask: the key at kpos sees the queries at or after it, a suffix
-      // of the tile's columns. (Columns past the chunk's end have LSE = +inf.)
+      // of the tile's columns. (Columns past the chunk's end hold -1e30 there.)
       int cf = 0;
       if (p.causal) {
         const int q0 = sq.base + qt * 128 * sq.stride;
@@ -537,20 +600,15 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       }
       tc_fence_after_sync();
       {
+        // dS^T = A^T * (dP^T - D); the products already subtracted D
         uint32_t r[64];
         tmem_ld_x64(tDP, r);
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(sl + 128 + c);
-          const float2 e0 = fmul2(make_float2(a[c], a[c + 1]),
-                                  make_float2(__uint_as_float(r[c]) - d4.x,
-                                              __uint_as_float(r[c + 1]) - d4.y));
-          const float2 e1 = fmul2(make_float2(a[c + 2], a[c + 3]),
-                                  make_float2(__uint_as_float(r[c + 2]) - d4.z,
-                                              __uint_as_float(r[c + 3]) - d4.w));
-          pk[c >> 1] = pack_bf16x2(e0.x, e0.y);
-          pk[(c >> 1) + 1] = pack_bf16x2(e1.x, e1.y);
+        for (int c = 0; c < 64; c += 2) {
+          const float2 e = fmul2(make_float2(a[c], a[c + 1]),
+                                 make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])));
+          pk[c >> 1] = pack_bf16x2(e.x, e.y);
         }
         tmem_st_x32(tDP, pk);
       }
@@ -967,14 +1025,16 @@ cudaError_t set_smem_once(K kernel, int bytes, std::atomic<unsigned long long>& 
 
 template <int D, bool ZIG>
 cudaError_t launch_dkdv_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                          const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+                          const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& text,
+                          cudaStream_t st) {
   static std::atomic<unsigned long long> done{0};
   const int smem = BwdSmem<D>::kAlloc;
   cudaError_t e = set_smem_once(bwd_dkdv_kernel<D, ZIG>, smem, done);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.B) * p.G * p.X * p.nt;
   if (grid <= 0) return cudaSuccess;
-  bwd_dkdv_kernel<D, ZIG><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tdo, tk, tv);
+  bwd_dkdv_kernel<D, ZIG><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(p, tq, tdo, tk, tv,
+                                                                                text);
   return cudaGetLastError();
 }
 
@@ -1007,13 +1067,14 @@ cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_dkdv(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+                            const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& text,
+                            cudaStream_t st) {
   const bool zig = p.layout == kZigzag;
   if (p.D == 64)
-    return zig ? launch_dkdv_d<64, true>(p, tq, tdo, tk, tv, st)
-               : launch_dkdv_d<64, false>(p, tq, tdo, tk, tv, st);
-  return zig ? launch_dkdv_d<128, true>(p, tq, tdo, tk, tv, st)
-             : launch_dkdv_d<128, false>(p, tq, tdo, tk, tv, st);
+    return zig ? launch_dkdv_d<64, true>(p, tq, tdo, tk, tv, text, st)
+               : launch_dkdv_d<64, false>(p, tq, tdo, tk, tv, text, st);
+  return zig ? launch_dkdv_d<128, true>(p, tq, tdo, tk, tv, text, st)
+             : launch_dkdv_d<128, false>(p, tq, tdo, tk, tv, text, st);
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,

@@ -47,6 +47,7 @@ struct RingParams {
 struct BwdParams {
   int32_t B, N, H, G, D, S, P, layout, causal;
   int32_t X, L, nt;
+  int32_t tiles;          // B * H * X * nt query tiles
   float scale;            // score scale (natural units)
   float scale_log2;       // scale * log2(e)
   uint64_t timeout_ns;    // limit of every device-side wait
@@ -58,6 +59,8 @@ struct BwdParams {
   const float* lse;
   // Per (batch, head, chunk, tile), 256 floats: LSE * log2(e) of the tile's 128
   // rows, then D = rowsum(dO * O); rows past the chunk's end hold +inf and 0.
+  // After the tiles * 256 floats: the extension rows (16 bf16 per query row) of
+  // -LSE/scale for every tile, then of -D, then one key-side tile of ones.
   float* ws;
   void* dq;
   void* dk;
@@ -88,7 +91,8 @@ int decode_chunk_keys(int S);
 // tq, tdo: [B,N,H,d] views; tk, tv: [B,N,G,d] views (as for the forward).
 cudaError_t launch_bwd_prep(const BwdParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                            const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+                            const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& text,
+                            cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                           const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 

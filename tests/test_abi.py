@@ -131,7 +131,9 @@ def test_decode_workspace_and_argument_checks(lib):
 ])
 def test_bwd_workspace_bytes(lib, layout, N, P, tiles_per_bh):
     pr = _pr(seqlen=N, P=P, layout=layout, heads=6, kv_heads=3, batch=2)
-    assert lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr)) == 2 * 6 * tiles_per_bh * 1024
+    # per query tile: 1 KiB of statistics and two 4 KiB extension tiles; one 4 KiB key-side tile
+    assert lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr)) == \
+        2 * 6 * tiles_per_bh * (1024 + 2 * 4096) + 4096
     assert lib.ring_attn_bwd_workspace_bytes(ctypes.byref(_pr(heads=3))) == 0
     assert lib.ring_attn_bwd_workspace_bytes(None) == 0
 

@@ -172,3 +172,13 @@ def test_bwd_c4_sampled():
     rows = sorted({0, 8191, 8192, N - 1} | set(rng.integers(0, N, 4).tolist()))
     keys = [N - 1, N - 128, N - 300]
     _sampled(w, rows, keys, groups=[3])
+
+
+def test_bwd_c3_striped_sampled():
+    w = WORKLOADS["c3"]
+    N = w.seqlen
+    rng = np.random.default_rng(13)
+    # first and last tokens of a few shards, plus random rows
+    rows = sorted({0, w.P - 1, w.P, N - 1, N - w.P} | set(rng.integers(0, N, 5).tolist()))
+    keys = [N - 1, N - 2, N - 17, N - 300]
+    _sampled(w, rows, keys, groups=[5])
