@@ -134,10 +134,10 @@ EncodeTiledFn encode_fn() {
 
 // Tensor map over a [B, N, heads, D] bf16 tensor seen as 5-D (innermost first):
 // contiguous (D, heads, S, P, B) — token = u*S + i; striped (D, heads, P, S, B) —
-// token = i*P + u. A box is 64 columns of one head over 128 local rows of one
-// shard, written to shared memory with the 128-byte swizzle.
+// token = i*P + u. A box is 64 columns of one head over box_rows local rows of
+// one shard, written to shared memory with the 128-byte swizzle.
 bool encode_rows(CUtensorMap* m, const void* base, int B, int N, int heads, int D, int S, int P,
-                 int layout) {
+                 int layout, int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t tok = static_cast<cuuint64_t>(heads) * D * 2;
@@ -155,7 +155,7 @@ bool encode_rows(CUtensorMap* m, const void* base, int B, int N, int heads, int 
     dims[3] = P;
     strides[1] = tok;
     strides[2] = tok * S;
-    box[2] = 128;
+    box[2] = static_cast<cuuint32_t>(box_rows);
     box[3] = 1;
   } else {
     dims[2] = P;
@@ -163,7 +163,7 @@ bool encode_rows(CUtensorMap* m, const void* base, int B, int N, int heads, int 
     strides[1] = tok;
     strides[2] = tok * P;
     box[2] = 1;
-    box[3] = 128;
+    box[3] = static_cast<cuuint32_t>(box_rows);
   }
   dims[4] = B;
   strides[3] = tok * N;
@@ -200,11 +200,9 @@ ra_status check_step_args(const ra_problem* pr, int32_t s, const void* q, const 
   return RA_OK;
 }
 
-// Number of partials the decode phase writes (one per shard and key chunk).
+// Number of partials the decode phase writes (one per shard segment and key chunk).
 int64_t decode_parts(const ra_problem* pr) {
-  const int S = pr->seqlen / pr->P;
-  const int chunk = decode_chunk_keys(S);
-  return static_cast<int64_t>(pr->P) * ((S + chunk - 1) / chunk);
+  return ra::decode_parts(pr->seqlen / pr->P, pr->P, pr->layout);
 }
 
 size_t decode_workspace(const ra_problem* pr, int32_t n_q) {
@@ -496,7 +494,13 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
   float* o_parts = static_cast<float*>(workspace);
   float* lse_parts = o_parts + static_cast<size_t>(parts) * pr->batch * n_q * pr->heads * pr->head_dim;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_partials(p, n_q, q_pos0, o_parts, lse_parts, cs);
+  // K/V tiles of 32 keys; zigzag tiles by chunk: the contiguous view over 2P chunks
+  const int ml = p.layout == kZigzag ? kContiguous : p.layout;
+  CUtensorMap tk, tv;
+  if (!encode_rows(&tk, k, p.B, p.N, p.G, p.D, p.L, p.X, ml, 32) ||
+      !encode_rows(&tv, v, p.B, p.N, p.G, p.D, p.L, p.X, ml, 32))
+    return RA_ERR_CUDA;
+  cudaError_t e = launch_decode_partials(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, cs);
   if (e != cudaSuccess) return RA_ERR_CUDA;
   return launch_result(launch_merge(static_cast<int>(parts), pr->batch, n_q, pr->heads,
                                     pr->head_dim, o_parts, lse_parts, o, lse, cs));

@@ -1,26 +1,28 @@
 // Pass-Q decode over the virtual ring: a few query rows attend to a KV cache that
 // stays sharded and stationary. Every virtual device u scores the queries against
-// its own shard only and leaves a partial (O_u, LSE_u); the partials are combined
-// by the merge kernel (merge.cu).
+// its own shard only and leaves partials (O, LSE); the partials are combined by
+// the merge kernel (merge.cu).
 //  * Transformer Math "Ring Attention" (aicassindra), "The ring is a prefill
 //    algorithm": broadcast the single query to all P devices, each computes a
 //    partial (m, l, o) against its shard, one small reduction combines them.
 //  * "Part 4: Ring Attention" (Fofadiya) §4.9.4.4: pass-Q decode.
 //
 // The partial phase is HBM-bound: each (batch, kv head) reads its K/V rows once,
-// and all query rows of the GQA group (heads of the group x decode tokens) share
-// them. A CTA owns RB query rows of one kv head and a chunk of keys of one shard
-// (a shard is cut into chunks so that a small batch still fills the GPU; every
-// chunk is one more partial for the merge).
+// and all query rows of the GQA group (heads of the group x decode tokens, up to
+// 16 per CTA) share them. A CTA owns those rows and a chunk of keys of one
+// segment of one shard (a shard is cut into chunks so that a small batch still
+// fills the GPU; every chunk is one more partial for the merge).
 //
-// Inside a CTA every warp streams its own groups of KG keys through a private
-// multi-stage cp.async pipeline in shared memory (16 KiB of loads in flight per
-// warp); lane l then reads d/32 consecutive columns of each K and V row, and those
-// registers serve all RB query rows. The
-// RB x KG partial dot products of a group are summed across lanes with a
-// butterfly reduce-scatter that leaves lane l with the full score of pair
-// (key l / RB, row l % RB). Each warp keeps its own online-softmax state
-// (m, z, y) in fp32; the warps of the CTA merge theirs once at the end.
+// The two products are tensor-core MMAs of 16 rows (mma.m16n8k16, bf16 in, fp32
+// accumulate): with at most 16 query rows per kv head, a 16-row MMA fits the
+// problem, and the kernel issues a few instructions per 16 bytes of K/V instead
+// of one FMA per element. Each of the 4 warps owns every 4th 32-key tile of the
+// chunk and streams it through its own 3-stage ring of shared memory with TMA
+// (128-byte swizzle; ldmatrix reads the swizzled rows, K as it is for S = Q K^T
+// and V transposed for O += P V). The S accumulators become the A operand of the
+// P V product without leaving registers. Each warp keeps its own online-softmax
+// state (running max m, denominator l, output O) in fp32; the warps merge theirs
+// once at the end and write the chunk's normalised partial.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -31,299 +33,308 @@
 namespace ra {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;                    // per-warp TMA ring
+constexpr int kTileKeys = 32;
+constexpr int kRows = 16;                     // query rows per CTA: the M of one MMA
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s to let in-flight copies land on abort
 
-template <int EPL>
-struct RowLoad;
-template <>
-struct RowLoad<4> {   // d = 128: 4 bf16 per lane, one 8-byte load
-  static __device__ __forceinline__ void get(const __nv_bfloat16* row, int lane, float (&f)[4]) {
-    const uint2 w = __ldcs(reinterpret_cast<const uint2*>(row) + lane);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  }
-};
-template <>
-struct RowLoad<2> {   // d = 64: 2 bf16 per lane, one 4-byte load
-  static __device__ __forceinline__ void get(const __nv_bfloat16* row, int lane, float (&f)[2]) {
-    const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(row) + lane);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-    f[0] = a.x; f[1] = a.y;
-  }
+template <int D>
+struct DecSmem {
+  static constexpr int kHalf = kTileKeys * 128;          // 32 rows x 64 bf16 (128 B, swizzled)
+  static constexpr int kTile = (D / 64) * kHalf;         // one [32 x D] bf16 tile
+  static constexpr int kStage = 2 * kTile;               // K, then V
+  static constexpr int kRing = kWarps * kStages * kStage;
+  static constexpr int kBar = kRing;                     // mbarriers [warp][stage], abort flag
+  static constexpr int kBytes = kBar + 8 * kWarps * kStages + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  // after the loop the ring holds the warps' states: O [warp][row][D], m, l [warp][row]
+  static constexpr int kMergeO = 0;
+  static constexpr int kMergeM = kWarps * kRows * D * 4;
+  static constexpr int kMergeL = kMergeM + kWarps * kRows * 4;
+  static_assert(kMergeL + kWarps * kRows * 4 <= kRing, "merge area inside the ring");
 };
 
-template <int EPL>
-__device__ __forceinline__ void smem_cols(const __nv_bfloat16* row, int lane, float (&f)[EPL]) {
-  if constexpr (EPL == 4) {
-    const uint2 w = reinterpret_cast<const uint2*>(row)[lane];
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-  } else {
-    const uint32_t w = reinterpret_cast<const uint32_t*>(row)[lane];
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-    f[0] = a.x; f[1] = a.y;
-  }
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Four 8x8 bf16 matrices; lanes 8m .. 8m+7 give the row addresses of matrix m.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Shared address of the 16-byte unit holding columns [col, col + 8) of row `row`
+// in a [32 x D] tile stored as 64-column chunks with the 128-byte swizzle (the
+// unit index inside a 128-byte row is XORed with row mod 8).
+template <int D>
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int col) {
+  return tile + (col >> 6) * DecSmem<D>::kHalf + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
 }
 
-// Sum over the 32 lanes of 32 values. Slot s of lane l must hold the lane's
-// contribution to value (s XOR l); afterwards lane l holds the total of value l
-// in v[0]. With that slot order every level keeps the lower half of the slots and
-// sends the upper half, so no lane-dependent selects are needed.
-__device__ __forceinline__ void reduce_scatter32(float (&v)[32]) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-    for (int i = 0; i < o; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + o], o);
-  }
+// TMA box coordinates of 32 rows starting at row i0 of a chunk (the views of
+// ring_attn_decode: (d, G, L, X, B), or (d, G, P, S, B) striped).
+__device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                         int layout, int dchunk, int head, int chunk, int i0,
+                                         int bat) {
+  if (layout == kStriped)
+    tma_load_5d(dst, map, bar, dchunk * 64, head, chunk, i0, bat);
+  else
+    tma_load_5d(dst, map, bar, dchunk * 64, head, i0, chunk, bat);
 }
 
-constexpr int kWarpStageBytes = 8192;    // per-warp pipeline: 8 KiB of K/V in flight
+// grid: x = g * n_rowgroups + rowgroup, y = segment * n_chunks + chunk, z = batch * P + u
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_mma_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, int n_q, int q_pos0, int chunk,
+                  int n_rowgroups, int n_chunks, float* __restrict__ o_parts,
+                  float* __restrict__ lse_parts) {
+  using L = DecSmem<D>;
+  constexpr int KS = D / 16;   // k-steps of S = Q K^T
+  constexpr int NT = D / 8;    // 8-column tiles of O
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kWarps * kStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;   // MMA fragment coordinates
 
-template <int D, int RB>
-struct DecCfg {
-  static constexpr int KG = 32 / RB;                   // keys per group
-  static constexpr int kStage = KG * D * 2 * 2;        // K and V rows of one group, bf16
-  static constexpr int kStages = kWarpStageBytes / kStage;
-  static constexpr int kPipe = kWarps * kStages * kStage;
-  static constexpr int kMerge = kWarps * RB * (D + 2) * 4;
-  static constexpr int kXchg = kWarps * (32 + RB) * 4;   // per-warp probabilities, rescales
-  static constexpr int kSmem = kPipe + kMerge + kXchg;
-};
-
-// grid: x = (g * n_rowgroups + rowgroup), y = key chunk of the shard, z = batch * P + u
-template <int D, int RB>
-__global__ void __launch_bounds__(kThreads, 2)
-decode_partial_kernel(const RingParams p, int n_q, int q_pos0, int chunk, int n_rowgroups,
-                      float* __restrict__ o_parts, float* __restrict__ lse_parts) {
-  using C = DecCfg<D, RB>;
-  constexpr int EPL = D / 32;          // columns per lane
-  constexpr int KG = C::KG;            // KG * RB = 32 (key, row) pairs per group
-  constexpr int NS = C::kStages;
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __nv_bfloat16* pipe = reinterpret_cast<__nv_bfloat16*>(smem_raw + warp * NS * C::kStage);
-  float* sm_m = reinterpret_cast<float*>(smem_raw + C::kPipe);       // [kWarps][RB]
-  float* sm_z = sm_m + kWarps * RB;                                   // [kWarps][RB]
-  float* sm_y = sm_z + kWarps * RB;                                   // [kWarps][RB][D]
-  float* sm_p = reinterpret_cast<float*>(smem_raw + C::kPipe + C::kMerge) + warp * (32 + RB);
   const int g = blockIdx.x / n_rowgroups, rg = blockIdx.x % n_rowgroups;
-  const int c = blockIdx.y;
+  const int sidx = blockIdx.y / n_chunks, c = blockIdx.y % n_chunks;
   const int bat = blockIdx.z / p.P, u = blockIdx.z % p.P;
+  const int nseg = num_segs(p.layout);
   const int hpg = p.H / p.G;
   const int rows_total = hpg * n_q;
-  const int row0 = rg * RB;
-  const int n_rows = min(RB, rows_total - row0);
-  const int j_begin = c * chunk;
-  const int j_end = min(p.S, j_begin + chunk);
-  const int part = u * static_cast<int>(gridDim.y) + c;
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
-  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
+  const int row0 = rg * kRows;
+  const int n_rows = min(kRows, rows_total - row0);
+  const Seg sg = seg_of(p.layout, p.S, p.P, u, sidx);
+  const int j_begin = c * chunk;                     // segment-local key range of the chunk
+  const int j_end = min(sg.len, j_begin + chunk);
+  const int part = (u * nseg + sidx) * n_chunks + c;
 
   // Rows: row r of the CTA is query row rr = row0 + r of kv head g, i.e. head
-  // g*hpg + rr / n_q, decode token rr % n_q at global position q_pos0 + rr % n_q.
+  // g * hpg + rr / n_q, decode token rr % n_q at global position q_pos0 + rr % n_q.
+  // This thread's accumulator rows are gid and gid + 8.
+  const bool v_lo = gid < n_rows, v_hi = gid + 8 < n_rows;
+  const int qpos_lo = v_lo ? q_pos0 + (row0 + gid) % n_q : -1;
+  const int qpos_hi = v_hi ? q_pos0 + (row0 + gid + 8) % n_q : -1;
   int qpos_max = -1;
-#pragma unroll
-  for (int r = 0; r < RB; ++r)
-    if (r < n_rows) qpos_max = max(qpos_max, q_pos0 + (row0 + r) % n_q);
-  // keys of the chunk some row may see: a prefix of the chunk, except for zigzag
-  // shards whose chunk may span both halves (then the per-key rule alone decides)
-  const int n_vis = j_end <= j_begin ? 0
-                    : p.layout == kZigzag ? j_end - j_begin
-                                          : visible_prefix(p.layout, p.S, p.P, p.causal, u, j_begin,
-                                                           j_end - j_begin, qpos_max);
+  for (int r = 0; r < n_rows; ++r) qpos_max = max(qpos_max, q_pos0 + (row0 + r) % n_q);
+  // keys of the chunk some row may see: a prefix of it
+  const int n_vis = j_end > j_begin ? seg_visible(sg, p.causal, j_begin, j_end - j_begin, qpos_max) : 0;
   const int j_stop = j_begin + n_vis;
+  const int n_tiles = (n_vis + kTileKeys - 1) / kTileKeys;
+  const int mine = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
 
-  // This lane's query columns of every row, pre-scaled by scale * log2(e), with
-  // the rows in slot order: slot row i holds row i XOR (lane mod RB).
-  float qv[RB][EPL];
-#pragma unroll
-  for (int i = 0; i < RB; ++i) {
-    const int r = i ^ (lane % RB);
-    if (r < n_rows) {
+  // Q rows as A fragments of the k-steps (rows past the CTA's rows are zero)
+  uint32_t qa[KS][4];
+  {
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    auto qrow = [&](int r) -> const uint32_t* {
       const int rr = row0 + r, h = g * hpg + rr / n_q, t = rr % n_q;
-      float f[EPL];
-      RowLoad<EPL>::get(q + ((static_cast<size_t>(bat) * n_q + t) * p.H + h) * D, lane, f);
+      return reinterpret_cast<const uint32_t*>(q + ((static_cast<size_t>(bat) * n_q + t) * p.H + h) * D);
+    };
+    const uint32_t* ql = v_lo ? qrow(gid) : nullptr;
+    const uint32_t* qh = v_hi ? qrow(gid + 8) : nullptr;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) qv[i][e] = f[e] * p.scale_log2;
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) qv[i][e] = 0.f;
+    for (int kk = 0; kk < KS; ++kk) {
+      qa[kk][0] = v_lo ? ql[8 * kk + tig] : 0u;
+      qa[kk][1] = v_hi ? qh[8 * kk + tig] : 0u;
+      qa[kk][2] = v_lo ? ql[8 * kk + 4 + tig] : 0u;
+      qa[kk][3] = v_hi ? qh[8 * kk + 4 + tig] : 0u;
     }
   }
-  const int my_r = lane % RB;
-  const int my_k = lane / RB;
-  const int my_qpos = (my_r < n_rows) ? q_pos0 + (row0 + my_r) % n_q : -1;
 
-  float m_run = -INFINITY, z_run = 0.f;   // state of row my_r (same on all its lanes)
-  float acc[RB][EPL];
-#pragma unroll
-  for (int r = 0; r < RB; ++r)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[r][e] = 0.f;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(sbase + L::kBar + 8 * i, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  __syncthreads();
 
-  const size_t row_stride = static_cast<size_t>(p.G) * D;   // elements between tokens
-  const __nv_bfloat16* kb = k + (static_cast<size_t>(bat) * p.N * p.G + g) * D;
-  const __nv_bfloat16* vb = v + (static_cast<size_t>(bat) * p.N * p.G + g) * D;
-
-  // The warp's groups: keys [j_begin + (warp + kWarps * n) * KG, +KG), n = 0, 1, ...
-  const int n_groups_total = (n_vis + KG - 1) / KG;
-  const int n_mine = n_groups_total > warp ? (n_groups_total - warp + kWarps - 1) / kWarps : 0;
-  auto issue = [&](int n) {   // copy group n of this warp into stage n % NS (always commits)
-    if (n < n_mine) {
-      const int j0 = j_begin + (warp + kWarps * n) * KG;
-      __nv_bfloat16* st = pipe + (n % NS) * (C::kStage / 2);
-      constexpr int kPieces = 2 * KG * (D / 8);          // 16-byte pieces of K and V rows
+  auto bar = [&](int st) -> uint32_t { return sbase + L::kBar + 8 * (warp * kStages + st); };
+  auto ring = [&](int st) -> uint32_t { return sbase + (warp * kStages + st) * L::kStage; };
+  auto issue = [&](int n) {   // lane 0: this warp's n-th tile into stage n % kStages
+    const int st = n % kStages;
+    const int j0 = j_begin + (warp + kWarps * n) * kTileKeys;
+    mbar_arrive_expect_tx(bar(st), L::kStage);
 #pragma unroll
-      for (int i = lane; i < kPieces; i += 32) {
-        const int row = i / (D / 8), pc = i % (D / 8);   // rows [0, KG): K, [KG, 2KG): V
-        const int kk = row % KG;
-        const int j = j0 + kk;
-        __nv_bfloat16* dst = st + row * D + pc * 8;
-        if (j < j_stop) {
-          const size_t tok = static_cast<size_t>(pos_of(p.layout, p.S, p.P, u, j));
-          const __nv_bfloat16* src = (row < KG ? kb : vb) + tok * row_stride + pc * 8;
-          cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(dst)), src);
-        } else {
-          *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-        }
-      }
+    for (int dc = 0; dc < D / 64; ++dc) {
+      tma_rows(&tk, ring(st) + dc * L::kHalf, bar(st), p.layout, dc, g, sg.chunk, j0, bat);
+      tma_rows(&tv, ring(st) + L::kTile + dc * L::kHalf, bar(st), p.layout, dc, g, sg.chunk, j0, bat);
     }
-    cp_async_commit();
   };
-#pragma unroll
-  for (int n = 0; n < NS - 1; ++n) issue(n);
+  if (lane == 0)
+    for (int n = 0; n < min(kStages, mine); ++n) issue(n);
+  __syncwarp();
 
-  for (int n = 0; n < n_mine; ++n) {
-    issue(n + NS - 1);
-    cp_async_wait<NS - 1>();   // group n has landed (for this lane)
-    __syncwarp();              // ... and for every lane of the warp
-    const __nv_bfloat16* st = pipe + (n % NS) * (C::kStage / 2);
-    const int j0 = j_begin + (warp + kWarps * n) * KG;
-    // partial dot products of the 32 (key, row) pairs over this lane's columns, in
-    // slot order: slot kk*RB + i holds pair (key kk XOR lane/RB, row i XOR lane%RB)
-    float dots[32];
+  const float c2 = p.scale_log2;
+  float m_lo = -INFINITY, m_hi = -INFINITY;   // running max of the scaled scores (log2 units)
+  float l_lo = 0.f, l_hi = 0.f;               // this thread's share of the denominators
+  float o[NT][4];
 #pragma unroll
-    for (int kk = 0; kk < KG; ++kk) {
-      float kf[EPL];
-      smem_cols<EPL>(st + (kk ^ my_k) * D, lane, kf);
+  for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  const int lm = lane >> 3, li = lane & 7;    // ldmatrix: matrix and row of this lane's address
+  bool ok = true;
+  int consumed = 0;
+  for (int n = 0; n < mine; ++n) {
+    const int st = n % kStages;
+    if (!__all_sync(0xffffffffu, bounded_wait(bar(st), static_cast<uint32_t>(n / kStages) & 1,
+                                              p.timeout_ns, abort_flag))) {
+      ok = false;
+      break;
+    }
+    const uint32_t sK = ring(st), sV = sK + L::kTile;
+    const int j0 = j_begin + (warp + kWarps * n) * kTileKeys;
+
+    // S = Q K^T over the tile's 32 keys: four 8-key tiles
+    float s[4][4];
 #pragma unroll
-      for (int i = 0; i < RB; i += 2) {
-        float2 sacc = make_float2(0.f, 0.f);
+    for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e)
-          sacc = ffma2(make_float2(qv[i][e], qv[i + 1][e]), make_float2(kf[e], kf[e]), sacc);
-        dots[kk * RB + i] = sacc.x;
-        dots[kk * RB + i + 1] = sacc.y;
+    for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz<D>(sK, 8 * (2 * np + (lm >> 1)) + li, 16 * kk + 8 * (lm & 1)), b0, b1, b2, b3);
+        mma_16816(s[2 * np], qa[kk], b0, b1);
+        mma_16816(s[2 * np + 1], qa[kk], b2, b3);
       }
     }
-    reduce_scatter32(dots);
-    // lane owns pair (my_k, my_r): its score, masked when invisible
-    const int jj = j0 + my_k;
-    const bool vis = jj < j_stop && my_r < n_rows &&
-                     key_visible(p.layout, p.S, p.P, p.causal, u, jj, my_qpos);
-    const float s_own = vis ? dots[0] : -INFINITY;
-    // online softmax of each row over the group's keys (lanes of one row differ by RB)
-    float mx = s_own;
+    // scale to log2 units and mask: keys past the visible prefix, or after the row
+    float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
-    for (int o = RB; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = j0 + 8 * nt + 2 * tig + e;
+        const int kp = sg.base + j * sg.stride;
+        const bool in = j < j_stop;
+        s[nt][e] = (in && v_lo && (!p.causal || kp <= qpos_lo)) ? s[nt][e] * c2 : -INFINITY;
+        s[nt][2 + e] = (in && v_hi && (!p.causal || kp <= qpos_hi)) ? s[nt][2 + e] * c2 : -INFINITY;
+        mx_lo = fmaxf(mx_lo, s[nt][e]);
+        mx_hi = fmaxf(mx_hi, s[nt][2 + e]);
+      }
+    }
+    // the four lanes of a row hold its 32 scores
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    const float mu_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+    const float mu_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
     // exact rescale exp(m_old - m_new); a row that saw nothing yet has a zero state
-    const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_use);
-    const float pr = exp2f(s_own - m_use);   // 0 when masked
-    float ps = pr;
+    const float a_lo = ex2(m_lo - mu_lo), a_hi = ex2(m_hi - mu_hi);
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+    // probabilities, as the A fragments of the two 16-key steps of O += P V
+    uint32_t pa[2][4];
+    float pl = 0.f, ph = 0.f;
 #pragma unroll
-    for (int o = RB; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    if (m_new != -INFINITY) {
-      z_run = z_run * alpha + ps;
-      m_run = m_new;
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = ex2(s[nt][0] - mu_lo), p1 = ex2(s[nt][1] - mu_lo);
+      const float p2 = ex2(s[nt][2] - mu_hi), p3 = ex2(s[nt][3] - mu_hi);
+      pl += p0 + p1;
+      ph += p2 + p3;
+      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
     }
-    // y_r = alpha_r y_r + sum_k p(k, r) V_k on this lane's columns; the 32
-    // probabilities and the RB rescale factors go through the warp's smem slot
-    sm_p[lane] = pr;
-    if (lane < RB) sm_p[32 + lane] = (m_new == -INFINITY) ? 1.f : alpha;
+    l_lo = l_lo * a_lo + pl;
+    l_hi = l_hi * a_hi + ph;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      o[nt][0] *= a_lo;
+      o[nt][1] *= a_lo;
+      o[nt][2] *= a_hi;
+      o[nt][3] *= a_hi;
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(swz<D>(sV, 16 * ks + 8 * (lm & 1) + li, 8 * (2 * np + (lm >> 1))), b0, b1, b2,
+                      b3);
+        mma_16816(o[2 * np], pa[ks], b0, b1);
+        mma_16816(o[2 * np + 1], pa[ks], b2, b3);
+      }
+    }
+    consumed = n + 1;
+    __syncwarp();   // every lane has read the stage before it is refilled
+    if (lane == 0 && n + kStages < mine) issue(n + kStages);
     __syncwarp();
-    float pk[32];
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const float4 t4 = *reinterpret_cast<const float4*>(sm_p + i);
-      pk[i] = t4.x; pk[i + 1] = t4.y; pk[i + 2] = t4.z; pk[i + 3] = t4.w;
-    }
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-      const float a_r = sm_p[32 + r];
-#pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        const float2 t2 = fmul2(make_float2(acc[r][e], acc[r][e + 1]), make_float2(a_r, a_r));
-        acc[r][e] = t2.x;
-        acc[r][e + 1] = t2.y;
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < KG; ++kk) {
-      float vf[EPL];
-      smem_cols<EPL>(st + (KG + kk) * D, lane, vf);
-#pragma unroll
-      for (int r = 0; r < RB; ++r) {
-        const float pv = pk[kk * RB + r];
-#pragma unroll
-        for (int e = 0; e < EPL; e += 2) {
-          const float2 t2 = ffma2(make_float2(pv, pv), make_float2(vf[e], vf[e + 1]),
-                                  make_float2(acc[r][e], acc[r][e + 1]));
-          acc[r][e] = t2.x;
-          acc[r][e + 1] = t2.y;
-        }
-      }
-    }
-    __syncwarp();   // every lane is done with stage n before it is refilled
   }
-  cp_async_wait<0>();
+  if (!ok) {
+    if (lane == 0) {
+      atomicCAS(p.status, 0, static_cast<int>(RA_ERR_TIMEOUT));
+      *abort_flag = 1;
+      // let this warp's copies in flight land before the CTA exits
+      for (int n = consumed; n < min(mine, consumed + kStages); ++n)
+        bounded_wait(bar(n % kStages), static_cast<uint32_t>(n / kStages) & 1, kDrainNs, nullptr);
+    }
+    __syncwarp();
+  }
+  // full denominators of the thread's rows (the four lanes of a row)
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
 
-  // Merge the warps' states: rescale each to the CTA-wide max and add.
-  if (lane < RB) {
-    sm_m[warp * RB + lane] = m_run;
-    sm_z[warp * RB + lane] = z_run;
+  // Merge the warps' states through the ring memory: rescale each to the
+  // CTA-wide max and add.
+  __syncthreads();
+  float* sm_o = reinterpret_cast<float*>(smem + L::kMergeO);   // [warp][row][D]
+  float* sm_m = reinterpret_cast<float*>(smem + L::kMergeM);   // [warp][row]
+  float* sm_l = reinterpret_cast<float*>(smem + L::kMergeL);
+  if (tig == 0) {
+    sm_m[warp * kRows + gid] = m_lo;
+    sm_m[warp * kRows + gid + 8] = m_hi;
+    sm_l[warp * kRows + gid] = l_lo;
+    sm_l[warp * kRows + gid + 8] = l_hi;
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = 8 * nt + 2 * tig;
+    *reinterpret_cast<float2*>(sm_o + (warp * kRows + gid) * D + col) = make_float2(o[nt][0], o[nt][1]);
+    *reinterpret_cast<float2*>(sm_o + (warp * kRows + gid + 8) * D + col) =
+        make_float2(o[nt][2], o[nt][3]);
   }
   __syncthreads();
-#pragma unroll
-  for (int r = 0; r < RB; ++r) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * RB + r]);
-    const float mw = sm_m[warp * RB + r];
-    const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) sm_y[(warp * RB + r) * D + lane * EPL + e] = acc[r][e] * f;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < RB * D; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < kRows * D; idx += kThreads) {
     const int r = idx / D, col = idx % D;
     if (r >= n_rows) continue;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * RB + r]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * kRows + r]);
     float Z = 0.f, Y = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float mw = sm_m[w * RB + r];
-      Z += (mw == -INFINITY) ? 0.f : sm_z[w * RB + r] * exp2f(mw - M);
-      Y += sm_y[(w * RB + r) * D + col];
+      const float mw = sm_m[w * kRows + r];
+      const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      Z += f * sm_l[w * kRows + r];
+      Y += f * sm_o[(w * kRows + r) * D + col];
     }
     const int rr = row0 + r, h = g * hpg + rr / n_q, t = rr % n_q;
     const size_t oo = (((static_cast<size_t>(part) * p.B + bat) * n_q + t) * p.H + h) * D + col;
@@ -335,39 +346,51 @@ decode_partial_kernel(const RingParams p, int n_q, int q_pos0, int chunk, int n_
   }
 }
 
-template <int D, int RB>
-cudaError_t launch_rb(const RingParams& p, int n_q, int q_pos0, int chunk, float* o_parts,
-                      float* lse_parts, cudaStream_t st) {
+template <int D>
+cudaError_t launch_d(const RingParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int n_q,
+                     int q_pos0, float* o_parts, float* lse_parts, cudaStream_t st) {
   const int rows_total = (p.H / p.G) * n_q;
-  const int n_rowgroups = (rows_total + RB - 1) / RB;
-  const int n_chunks = (p.S + chunk - 1) / chunk;
-  const int smem = DecCfg<D, RB>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<D, RB>,
+  const int n_rowgroups = (rows_total + kRows - 1) / kRows;
+  const int nseg = num_segs(p.layout);
+  const int seg_len = p.S / nseg;
+  const int chunk = decode_chunk_keys(p.S, p.P, p.layout);
+  const int n_chunks = (seg_len + chunk - 1) / chunk;
+  const int smem = DecSmem<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.G * n_rowgroups, n_chunks, p.B * p.P);
-  decode_partial_kernel<D, RB><<<grid, kThreads, smem, st>>>(p, n_q, q_pos0, chunk, n_rowgroups,
-                                                             o_parts, lse_parts);
+  const dim3 grid(p.G * n_rowgroups, nseg * n_chunks, p.B * p.P);
+  decode_mma_kernel<D><<<grid, kThreads, smem, st>>>(p, tk, tv, n_q, q_pos0, chunk, n_rowgroups,
+                                                     n_chunks, o_parts, lse_parts);
   return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t launch_d(const RingParams& p, int n_q, int q_pos0, int chunk, float* o_parts,
-                     float* lse_parts, cudaStream_t st) {
-  const int rows_total = (p.H / p.G) * n_q;
-  if (rows_total <= 4) return launch_rb<D, 4>(p, n_q, q_pos0, chunk, o_parts, lse_parts, st);
-  return launch_rb<D, 8>(p, n_q, q_pos0, chunk, o_parts, lse_parts, st);
 }
 
 }  // namespace
 
-int decode_chunk_keys(int S) { return S <= 4096 ? S : 4096; }
+// Keys per chunk of a shard segment: 2048, or more when that would give more than
+// 1024 partials (the merge kernel's limit), rounded up to whole 32-key tiles.
+int decode_chunk_keys(int S, int P, int layout) {
+  const int nseg = num_segs(layout);
+  const int seg_len = S / nseg;
+  long long chunk = seg_len < 2048 ? seg_len : 2048;
+  const long long min_chunk = (static_cast<long long>(seg_len) * nseg * P + 1023) / 1024;
+  if (chunk < min_chunk) chunk = (min_chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
+  if (chunk > seg_len) chunk = seg_len;
+  return static_cast<int>(chunk < 1 ? 1 : chunk);
+}
 
-cudaError_t launch_decode_partials(const RingParams& p, int n_q, int q_pos0, float* o_parts,
+int decode_parts(int S, int P, int layout) {
+  const int nseg = num_segs(layout);
+  const int seg_len = S / nseg;
+  const int chunk = decode_chunk_keys(S, P, layout);
+  return P * nseg * ((seg_len + chunk - 1) / chunk);
+}
+
+cudaError_t launch_decode_partials(const RingParams& p, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, int n_q, int q_pos0, float* o_parts,
                                    float* lse_parts, cudaStream_t st) {
-  const int chunk = decode_chunk_keys(p.S);
-  return p.D == 64 ? launch_d<64>(p, n_q, q_pos0, chunk, o_parts, lse_parts, st)
-                   : launch_d<128>(p, n_q, q_pos0, chunk, o_parts, lse_parts, st);
+  return p.D == 64 ? launch_d<64>(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, st)
+                   : launch_d<128>(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, st);
 }
 
 }  // namespace ra

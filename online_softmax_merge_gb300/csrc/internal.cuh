@@ -81,11 +81,15 @@ cudaError_t launch_tile_classes(const RingParams& p, int u, int b, int8_t* class
                                 cudaStream_t st);
 cudaError_t launch_mask(const RingParams& p, int u, int b, uint8_t* mask, cudaStream_t st);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t st);
-// Pass-Q decode, phase 1: per-(shard, key chunk) partials into the workspace.
-cudaError_t launch_decode_partials(const RingParams& p, int n_q, int q_pos0, float* o_parts,
+// Pass-Q decode, phase 1: per-(shard segment, key chunk) partials into the
+// workspace. tk, tv: [B,N,G,d] views with 32-row boxes.
+cudaError_t launch_decode_partials(const RingParams& p, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, int n_q, int q_pos0, float* o_parts,
                                    float* lse_parts, cudaStream_t st);
-// Keys per chunk of a shard in the decode partial phase.
-int decode_chunk_keys(int S);
+// Keys per chunk of a shard segment in the decode partial phase, and the number
+// of partials (P x segments x chunks per segment).
+int decode_chunk_keys(int S, int P, int layout);
+int decode_parts(int S, int P, int layout);
 
 // Backward: statistics pass, then the dK/dV and dQ tensor-core kernels.
 // tq, tdo: [B,N,H,d] views; tk, tv: [B,N,G,d] views (as for the forward).
