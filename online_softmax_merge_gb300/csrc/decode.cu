@@ -10,8 +10,8 @@
 // The partial phase is HBM-bound: each (batch, kv head) reads its K/V rows once,
 // and all query rows of the GQA group (heads of the group x decode tokens, up to
 // 16 per CTA) share them. A CTA owns those rows and a chunk of keys of one
-// segment of one shard (a shard is cut into chunks so that a small batch still
-// fills the GPU; every chunk is one more partial for the merge).
+// segment of one shard (long shards are cut into chunks of up to 8192 keys;
+// every chunk is one more partial for the merge).
 //
 // The two products are tensor-core MMAs of 16 rows (mma.m16n8k16, bf16 in, fp32
 // accumulate): with at most 16 query rows per kv head, a 16-row MMA fits the
@@ -367,12 +367,14 @@ cudaError_t launch_d(const RingParams& p, const CUtensorMap& tk, const CUtensorM
 
 }  // namespace
 
-// Keys per chunk of a shard segment: 2048, or more when that would give more than
-// 1024 partials (the merge kernel's limit), rounded up to whole 32-key tiles.
+// Keys per chunk of a shard segment: up to 8192 (a CTA's start-up — barriers, Q
+// rows, filling the TMA rings — is a few microseconds, so long chunks pay even
+// when the last wave of CTAs is partly empty), or more when that would give more
+// than 1024 partials (the merge kernel's limit), rounded up to whole 32-key tiles.
 int decode_chunk_keys(int S, int P, int layout) {
   const int nseg = num_segs(layout);
   const int seg_len = S / nseg;
-  long long chunk = seg_len < 2048 ? seg_len : 2048;
+  long long chunk = seg_len < 8192 ? seg_len : 8192;
   const long long min_chunk = (static_cast<long long>(seg_len) * nseg * P + 1023) / 1024;
   if (chunk < min_chunk) chunk = (min_chunk + kTileKeys - 1) / kTileKeys * kTileKeys;
   if (chunk > seg_len) chunk = seg_len;
