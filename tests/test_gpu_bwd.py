@@ -37,6 +37,13 @@ CASES = [
     Workload("tiny", 1, 8, 2, 1, 64, 2, "contiguous", True, 207),
     Workload("stress", 1, 4 * 256, 4, 2, 128, 4, "contiguous", True, 9,
              stress_frac=0.05, stress_factor=8.0),
+    # degenerate shapes: every token its own shard, a single partial tile, odd tile
+    # counts with MHA, one-token zigzag chunks
+    Workload("s1-every-token-a-shard", 1, 64, 2, 1, 128, 64, "striped", True, 212),
+    Workload("tiny-noncausal", 1, 5, 2, 2, 128, 1, "contiguous", False, 213),
+    Workload("mha-odd-tiles", 1, 3 * (5 * 128 + 8), 3, 3, 128, 3, "contiguous", True, 214),
+    Workload("zigzag-s2", 1, 64, 4, 2, 128, 32, "zigzag", True, 215),
+    Workload("d64-striped-causal", 1, 4 * 300, 2, 2, 64, 4, "striped", True, 216),
 ]
 
 

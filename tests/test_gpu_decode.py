@@ -38,6 +38,8 @@ CASES = [
     (1, 2 * 4500, 16, 1, 128, 2, "striped", True, 3, None),      # 48 rows: two row groups
     (1, 4 * 2600, 8, 2, 128, 2, "zigzag", True, 2, 5000),        # zigzag, chunks span halves
     (2, 8 * 512, 4, 1, 64, 4, "zigzag", True, 1, None),
+    (1, 4 * 1100, 8, 2, 128, 4, "contiguous", True, 40, None),   # 160 rows: ten row groups
+    (1, 2 * 9000, 4, 1, 128, 2, "contiguous", True, 1, None),    # 9000-key shards: two chunks
 ]
 
 
