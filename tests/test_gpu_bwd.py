@@ -189,3 +189,14 @@ def test_bwd_c3_striped_sampled():
     rows = sorted({0, w.P - 1, w.P, N - 1, N - w.P} | set(rng.integers(0, N, 5).tolist()))
     keys = [N - 1, N - 2, N - 17, N - 300]
     _sampled(w, rows, keys, groups=[5])
+
+
+def test_bwd_c5_one_million_tokens_sampled():
+    """The largest workload (1,048,576 tokens, striped over 64 shards): the backward
+    from the GPU forward, checked on sampled query rows and on the last keys."""
+    w = WORKLOADS["c5"]
+    N = w.seqlen
+    rng = np.random.default_rng(15)
+    rows = sorted({0, w.P, N - 1} | set(rng.integers(0, N, 3).tolist()))
+    keys = [N - 1, N - 65, N - 200]
+    _sampled(w, rows, keys, groups=[7])
