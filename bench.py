@@ -56,7 +56,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "ring_tc_kernel": ["ring_tc.cu", "ptx.cuh", "shardmap.cuh"],
+    "ring_tc_kernel": ["ring_tc.cu", "ptx.cuh", "shardmap.cuh", "views.cuh"],
     "merge_kernel": ["merge.cu"],
 }
 

@@ -58,6 +58,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "shardmap.cuh"
+#include "views.cuh"
 
 namespace ra {
 namespace {
@@ -115,16 +116,6 @@ __device__ __forceinline__ void record_failure(const BwdParams& p, volatile int*
   *abort_flag = 1;
 }
 
-// TMA box coordinates of 128 rows starting at row i0 of a chunk (see the
-// forward's tensor maps: (d, heads, L, X, B), or (d, heads, P, S, B) striped).
-__device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, uint32_t bar,
-                                         int layout, int dchunk, int head, int chunk, int i0,
-                                         int bat) {
-  if (layout == kStriped)
-    tma_load_5d(dst, map, bar, dchunk * 64, head, chunk, i0, bat);
-  else
-    tma_load_5d(dst, map, bar, dchunk * 64, head, i0, chunk, bat);
-}
 
 // 2-D tiled TMA load (the extension tiles: 16 bf16 x 128 rows, 32-byte swizzle).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,

@@ -29,6 +29,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "shardmap.cuh"
+#include "views.cuh"
 
 namespace ra {
 namespace {
@@ -87,16 +88,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int col) {
   return tile + (col >> 6) * DecSmem<D>::kHalf + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
 }
 
-// TMA box coordinates of 32 rows starting at row i0 of a chunk (the views of
-// ring_attn_decode: (d, G, L, X, B), or (d, G, P, S, B) striped).
-__device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, uint32_t bar,
-                                         int layout, int dchunk, int head, int chunk, int i0,
-                                         int bat) {
-  if (layout == kStriped)
-    tma_load_5d(dst, map, bar, dchunk * 64, head, chunk, i0, bat);
-  else
-    tma_load_5d(dst, map, bar, dchunk * 64, head, i0, chunk, bat);
-}
 
 // grid: x = g * n_rowgroups + rowgroup, y = segment * n_chunks + chunk, z = batch * P + u
 template <int D>

@@ -37,6 +37,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "shardmap.cuh"
+#include "views.cuh"
 
 namespace ra {
 namespace {
@@ -137,18 +138,6 @@ __device__ __forceinline__ int kv_tiles(const RingParams& p, const Seg& g, int q
   return (n + 127) >> 7;
 }
 
-// TMA box coordinates (innermost first) of 128 rows starting at row i0 of a
-// segment: the tensor maps view [B, N, heads, d] as (d, heads, L, X, B) for the
-// contiguous and zigzag layouts (X chunks of L tokens; the segment's chunk index)
-// and as (d, heads, P, S, B) for the striped one (the segment's shard).
-__device__ __forceinline__ void tma_rows(const CUtensorMap* map, uint32_t dst, uint32_t bar,
-                                         int layout, int dchunk, int head, int chunk, int i0,
-                                         int bat) {
-  if (layout == kStriped)
-    tma_load_5d(dst, map, bar, dchunk * 64, head, chunk, i0, bat);
-  else
-    tma_load_5d(dst, map, bar, dchunk * 64, head, i0, chunk, bat);
-}
 
 __device__ __forceinline__ void record_failure(const RingParams& p, volatile int* abort_flag) {
   atomicCAS(p.status, 0, static_cast<int>(RA_ERR_TIMEOUT));
