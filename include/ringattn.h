@@ -105,6 +105,31 @@ typedef struct {
 ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const void* v,
                         void* o, float* lse, void* stream);
 
+/* The full ring forward for inputs that live in HOST memory: q, k, v are read
+ * from, o and lse written to, host memory (page-locked memory lets the copies
+ * overlap the kernels; pageable memory also works, with the copies serialised).
+ * The batch goes through the GPU one sequence at a time in two device slots of
+ * the workspace: while sequence b is computed on `stream`, the inputs of b + 1
+ * travel in and the outputs of b - 1 travel out on `copy_stream`, so only the
+ * first sequence's inputs and the last one's outputs are not hidden behind
+ * compute. Each sequence is exactly a ring_attn_fwd call (the results are the
+ * same bit for bit). Work enqueued on `stream` before the call happens before
+ * any of its copies, and `stream` completes only once the outputs are in host
+ * memory, so synchronising `stream` is enough. The call returns after enqueuing;
+ * it creates and releases its ordering events itself. There is no counterpart in
+ * the pages: this is an interface choice of this library (host-resident inputs,
+ * e.g. in the CPU memory of a Grace host).
+ * q, k, v, o, lse: host pointers in the shapes of ring_attn_fwd. workspace:
+ * device memory of at least ring_attn_fwd_host_workspace_bytes(p) bytes,
+ * 16-byte aligned, overwritten. copy_stream may equal stream (no overlap). */
+ra_status ring_attn_fwd_host(const ra_problem* p, const void* q, const void* k, const void* v,
+                             void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream, void* copy_stream);
+
+/* Bytes of device workspace ring_attn_fwd_host needs: two sequences' q, k, v, o,
+ * lse (one if the batch is 1), each rounded up to 256 bytes. Pure host code. */
+size_t ring_attn_fwd_host_workspace_bytes(const ra_problem* p);
+
 /* One ring step for all virtual devices at once: device u folds shard
  * b = (u - s) mod P into the running state (m, z, y) of its own query rows.
  * first != 0 starts from the empty state (m = -inf, z = 0, y = 0) and ignores

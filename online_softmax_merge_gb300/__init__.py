@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import (LAYOUTS, RA_ERR_CUDA, RA_ERR_INVALID_ARG, RA_ERR_TIMEOUT,  # noqa: F401
                    RA_ERR_UNSUPPORTED, RA_OK, TILE, RingAttnError, check, load)
 
-__all__ = ["fwd", "bwd", "bwd_workspace_bytes", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
+__all__ = ["fwd", "fwd_host", "fwd_host_workspace_bytes", "bwd", "bwd_workspace_bytes", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
            "tile_classes", "mask", "last_error", "selftest_timeout", "problem", "RingAttnError",
            "empty_state", "LAYOUTS", "TILE"]
 
@@ -83,6 +83,74 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str =
     with torch.cuda.device(q.device):
         check("ring_attn_fwd", lib.ring_attn_fwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v),
                                                  _ptr(out), _ptr(lse), _stream(q.device)))
+    return out, lse
+
+
+def _need_host(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+_COPY_STREAMS = {}
+
+
+def fwd_host_workspace_bytes(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int,
+                             P: int, layout: str = "contiguous", causal: bool = True) -> int:
+    """Device workspace bytes ring_attn_fwd_host needs."""
+    lib = load()
+    pr = problem(batch, seqlen, heads, kv_heads, head_dim, P, causal, layout)
+    return int(lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr)))
+
+
+def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
+             layout: str = "contiguous", causal: bool = True, scale: float = 0.0,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, device=None,
+             copy_stream: Optional[torch.cuda.Stream] = None):
+    """Ring forward for host tensors (ring_attn_fwd_host): q [B, N, H, d], k, v
+    [B, N, G, d] bf16 on the CPU (pinned for overlap); returns host (O, LSE). Runs
+    on `device` (default: the current CUDA device) and its current stream; copies
+    go on copy_stream (default: one cached side stream per device)."""
+    lib = load()
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, N, H, d] and k, v [B, N, G, d]")
+    B, N, H, d = q.shape
+    G = k.shape[2]
+    _need_host(q, "q", torch.bfloat16, (B, N, H, d))
+    _need_host(k, "k", torch.bfloat16, (B, N, G, d))
+    _need_host(v, "v", torch.bfloat16, (B, N, G, d))
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    pr = problem(B, N, H, G, d, P, causal, layout, scale)
+    need = int(lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    _need_host(out, "out", torch.bfloat16, (B, N, H, d))
+    _need_host(lse, "lse", torch.float32, (B, H, N))
+    if copy_stream is None:
+        copy_stream = _COPY_STREAMS.get(dev.index)
+        if copy_stream is None:
+            copy_stream = torch.cuda.Stream(device=dev)
+            _COPY_STREAMS[dev.index] = copy_stream
+    with torch.cuda.device(dev):
+        check("ring_attn_fwd_host", lib.ring_attn_fwd_host(
+            ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev),
+            ctypes.c_void_p(copy_stream.cuda_stream)))
     return out, lse
 
 

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <new>
 
 #include "internal.cuh"
 #include "shardmap.cuh"
@@ -236,6 +237,25 @@ bool encode_ext(CUtensorMap* m, const void* base, int64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Device slot of ring_attn_fwd_host: one sequence's q, k, v, o, lse, each
+// rounded up to 256 bytes.
+struct HostSlot {
+  size_t q, kv, o, lse, total;
+};
+HostSlot host_slot(const ra_problem* pr) {
+  auto r256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  HostSlot s;
+  s.q = r256(static_cast<size_t>(pr->seqlen) * pr->heads * pr->head_dim * 2);
+  s.kv = r256(static_cast<size_t>(pr->seqlen) * pr->kv_heads * pr->head_dim * 2);
+  s.o = s.q;
+  s.lse = r256(static_cast<size_t>(pr->heads) * pr->seqlen * sizeof(float));
+  s.total = s.q + 2 * s.kv + s.o + s.lse;
+  return s;
+}
+size_t fwd_host_workspace(const ra_problem* pr) {
+  return host_slot(pr).total * static_cast<size_t>(pr->batch < 2 ? pr->batch : 2);
+}
+
 }  // namespace
 
 extern "C" {
@@ -260,6 +280,93 @@ ra_status ring_attn_fwd(const ra_problem* pr, const void* q, const void* k, cons
   p.lse = lse;
   p.status = d->status;
   return run_tc(p, static_cast<cudaStream_t>(stream));
+}
+
+size_t ring_attn_fwd_host_workspace_bytes(const ra_problem* pr) {
+  if (check_problem(pr) != RA_OK) return 0;
+  return fwd_host_workspace(pr);
+}
+
+ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k, const void* v,
+                             void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             void* stream, void* copy_stream) {
+  ra_status st = check_problem(pr);
+  if (st != RA_OK) return st;
+  if (!q || !k || !v || !o || !lse || !workspace || !aligned16(workspace))
+    return RA_ERR_INVALID_ARG;
+  if (workspace_bytes < fwd_host_workspace(pr)) return RA_ERR_INVALID_ARG;
+  DevInfo* d = nullptr;
+  if ((st = current_device(&d)) != RA_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+  const HostSlot hs = host_slot(pr);
+  // one sequence: a B = 1 problem with the same shapes
+  ra_problem one = *pr;
+  one.batch = 1;
+  RingParams p;
+  fill_params(&one, &p);
+  p.s_begin = 0;
+  p.s_end = p.P;
+  p.status = d->status;
+  const size_t qn = static_cast<size_t>(pr->seqlen) * pr->heads * pr->head_dim * 2;
+  const size_t kn = static_cast<size_t>(pr->seqlen) * pr->kv_heads * pr->head_dim * 2;
+  const size_t ln = static_cast<size_t>(pr->heads) * pr->seqlen * sizeof(float);
+  const int B = pr->batch;
+  // events: start (stream -> copy_stream), inputs in[b], kernel done k[b], end
+  const int n_ev = 2 + 2 * B;
+  cudaEvent_t* ev = new (std::nothrow) cudaEvent_t[n_ev];
+  if (ev == nullptr) return RA_ERR_CUDA;
+  int made = 0;
+  cudaError_t e = cudaSuccess;
+  for (; made < n_ev && e == cudaSuccess; ++made)
+    e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+  if (e != cudaSuccess) --made;
+  cudaEvent_t ev_start = ev[0], ev_end = ev[1];
+  auto ev_in = [&](int b) { return ev[2 + b]; };
+  auto ev_k = [&](int b) { return ev[2 + B + b]; };
+  auto slot = [&](int b) { return static_cast<uint8_t*>(workspace) + (b % 2) * hs.total; };
+  auto h2d = [&](int b) -> cudaError_t {
+    uint8_t* s0 = slot(b);
+    cudaError_t r = cudaMemcpyAsync(s0, static_cast<const uint8_t*>(q) + b * qn, qn,
+                                    cudaMemcpyHostToDevice, xs);
+    if (r == cudaSuccess)
+      r = cudaMemcpyAsync(s0 + hs.q, static_cast<const uint8_t*>(k) + b * kn, kn,
+                          cudaMemcpyHostToDevice, xs);
+    if (r == cudaSuccess)
+      r = cudaMemcpyAsync(s0 + hs.q + hs.kv, static_cast<const uint8_t*>(v) + b * kn, kn,
+                          cudaMemcpyHostToDevice, xs);
+    if (r == cudaSuccess) r = cudaEventRecord(ev_in(b), xs);
+    return r;
+  };
+  if (e == cudaSuccess) e = cudaEventRecord(ev_start, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, ev_start, 0);
+  for (int b = 0; b < B && b < 2 && e == cudaSuccess; ++b) e = h2d(b);
+  for (int b = 0; b < B && e == cudaSuccess; ++b) {
+    uint8_t* s0 = slot(b);
+    e = cudaStreamWaitEvent(cs, ev_in(b), 0);
+    if (e != cudaSuccess) break;
+    p.q = s0;
+    p.k = s0 + hs.q;
+    p.v = s0 + hs.q + hs.kv;
+    p.o = s0 + hs.q + 2 * hs.kv;
+    p.lse = reinterpret_cast<float*>(s0 + hs.q + 2 * hs.kv + hs.o);
+    if ((st = run_tc(p, cs)) != RA_OK) break;
+    e = cudaEventRecord(ev_k(b), cs);
+    // outputs of b out, then (its slot free) the inputs of b + 2 in
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, ev_k(b), 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(o) + b * qn, p.o, qn, cudaMemcpyDeviceToHost, xs);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + b * ln, p.lse, ln,
+                          cudaMemcpyDeviceToHost, xs);
+    if (e == cudaSuccess && b + 2 < B) e = h2d(b + 2);
+  }
+  if (e == cudaSuccess && st == RA_OK) e = cudaEventRecord(ev_end, xs);
+  if (e == cudaSuccess && st == RA_OK) e = cudaStreamWaitEvent(cs, ev_end, 0);
+  for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);   // released once they complete
+  delete[] ev;
+  if (st != RA_OK) return st;
+  return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
 ra_status ring_attn_step(const ra_problem* pr, int32_t s, int32_t first, const void* q,

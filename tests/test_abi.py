@@ -153,3 +153,23 @@ def test_bwd_argument_checks(lib):
     assert lib.ring_attn_bwd(ctypes.byref(_pr(head_dim=96)), *[FAKE] * 10, need, None) == \
         _lib.RA_ERR_UNSUPPORTED
     assert lib.ring_attn_bwd(None, *[FAKE] * 10, need, None) == _lib.RA_ERR_INVALID_ARG
+
+
+def test_fwd_host_workspace_and_argument_checks(lib):
+    pr = _pr(batch=3, seqlen=1000, heads=4, kv_heads=2, head_dim=128, P=4)
+    r = lambda x: (x + 255) // 256 * 256
+    slot = r(1000 * 4 * 128 * 2) * 2 + r(1000 * 2 * 128 * 2) * 2 + r(4 * 1000 * 4)
+    assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr)) == 2 * slot
+    one = _pr(batch=1, seqlen=1000, heads=4, kv_heads=2, head_dim=128, P=4)
+    assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(one)) == slot
+    assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(_pr(heads=3))) == 0
+    ptrs = [FAKE] * 5
+    assert lib.ring_attn_fwd_host(ctypes.byref(pr), *ptrs, FAKE, 2 * slot - 1, None, None) == \
+        _lib.RA_ERR_INVALID_ARG                     # workspace too small
+    assert lib.ring_attn_fwd_host(ctypes.byref(pr), *ptrs, ctypes.c_void_p(0x10008), 2 * slot,
+                                  None, None) == _lib.RA_ERR_INVALID_ARG   # misaligned workspace
+    for i in range(5):
+        bad = list(ptrs)
+        bad[i] = None
+        assert lib.ring_attn_fwd_host(ctypes.byref(pr), *bad, FAKE, 2 * slot, None, None) == \
+            _lib.RA_ERR_INVALID_ARG

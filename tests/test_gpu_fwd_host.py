@@ -1,0 +1,48 @@
+"""ring_attn_fwd_host: the ring forward for inputs in host memory, pipelined one
+sequence at a time through two device slots. Each sequence is a ring_attn_fwd call,
+so the results must equal the device path bit for bit."""
+import pytest
+import torch
+
+from online_softmax_merge_gb300.inputs import Workload, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+ra = pytest.importorskip("online_softmax_merge_gb300")
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.mark.parametrize("B,layout,pinned", [(3, "contiguous", True), (1, "striped", True),
+                                             (2, "zigzag", False), (4, "striped", False)])
+def test_host_forward_equals_device_forward(B, layout, pinned):
+    w = Workload("host", B, 4 * (2 * 128 + 40), 4, 2, 128, 4, layout, True, 400 + B)
+    q, k, v = make_qkv(w)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_h, l_h = ra.fwd_host(q, k, v, w.P, w.layout, w.causal, device=DEV)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    o_d, l_d = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())
+
+
+@pytest.mark.parametrize("same_stream", [True, False])
+def test_host_forward_after_prior_work_on_the_stream(same_stream):
+    """The call's copies start only after work already enqueued on the stream (here:
+    a device-to-host write into the host input the call then reads), whether the
+    copies share the compute stream or run on the side stream."""
+    w = Workload("host1", 2, 2 * 300, 2, 1, 64, 2, "contiguous", True, 410)
+    q, k, v = (t.pin_memory() for t in make_qkv(w))
+    q_dev = torch.randn(q.shape, device=DEV).to(torch.bfloat16)
+    cur = torch.cuda.current_stream(DEV)
+    torch.cuda._sleep(20_000_000)                 # keep the stream busy for a while
+    q.copy_(q_dev, non_blocking=True)             # enqueued on the current stream
+    o_h, l_h = ra.fwd_host(q, k, v, w.P, w.layout, w.causal, device=DEV,
+                           copy_stream=cur if same_stream else None)
+    torch.cuda.synchronize()
+    o_d, l_d = ra.fwd(q_dev, k.to(DEV), v.to(DEV), w.P, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())
