@@ -33,13 +33,16 @@
  *  "The causal masking complication").
  *
  *  Pointers named q,k,v,o,lse,m,z,y,o_parts,lse_parts,dout,dq,dk,dv,workspace
- *  are DEVICE pointers,
- *  allocated and owned by the caller, 16-byte aligned. The library allocates
- *  no device memory; it keeps one status word in static device memory per GPU.
- *  `stream` is a cudaStream_t (NULL = legacy default stream); every call that
- *  takes one is asynchronous on it. Calls on one stream are ordered; the
- *  library holds no per-call host state, so concurrent calls on different
- *  streams are safe when their output buffers do not overlap.
+ *  are DEVICE pointers, allocated and owned by the caller, 16-byte aligned —
+ *  except the host pointers of ring_attn_fwd_host and of the host shard map,
+ *  which say so. The library allocates no device memory; its static device
+ *  memory is one status word per GPU and the fixed scratch array of
+ *  ring_attn_decode_noalloc. `stream` is a cudaStream_t (NULL = legacy default
+ *  stream); every call that takes one is asynchronous on it. Calls on one
+ *  stream are ordered; the library holds no per-call host state beyond the
+ *  ordering events ring_attn_fwd_host creates and releases itself, so
+ *  concurrent calls on different streams are safe when their output buffers
+ *  (and workspaces) do not overlap.
  *
  *  Errors: argument errors are returned synchronously before any launch and
  *  nothing is written. RA_ERR_CUDA means a CUDA call (launch or tensor-map
