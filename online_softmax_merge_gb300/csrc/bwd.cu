@@ -291,10 +291,14 @@ __device__ __forceinline__ KUnit decode_kunit(const BwdParams& p, int idx) {
   const int bg = idx / per_bg;
   const int r = idx - bg * per_bg;
   // Earliest key positions first: under a causal mask they meet the most queries.
+  // Striped tiles go in blocks of 4 tile indices per shard, so that the CTAs
+  // resident at one time cover few shards and reread the same Q/dO tiles from L2.
   int c, kt;
   if (p.layout == kStriped) {
-    kt = r / p.P;
-    c = r - kt * p.P;
+    const int QB = (p.nt % 4 == 0) ? 4 : 1;
+    const int blk = r / (QB * p.P), rem = r - blk * QB * p.P;
+    c = rem / QB;
+    kt = blk * QB + (rem - c * QB);
   } else {
     c = r / p.nt;
     kt = r - c * p.nt;
@@ -664,11 +668,14 @@ __device__ __forceinline__ QUnit decode_qunit(const BwdParams& p, int idx) {
   const int bh = idx / per_bh;
   const int r = idx - bh * per_bh;
   // Latest query positions first: under a causal mask they see the most keys.
+  // Striped tiles go in blocks of 4 tile indices per shard (as in the forward).
   const int key = per_bh - 1 - r;
   int c, qt;
   if (p.layout == kStriped) {
-    qt = key / p.P;
-    c = key - qt * p.P;
+    const int QB = (p.nt % 4 == 0) ? 4 : 1;
+    const int blk = key / (QB * p.P), rem = key - blk * QB * p.P;
+    c = rem / QB;
+    qt = blk * QB + (rem - c * QB);
   } else {
     c = key / p.nt;
     qt = key - c * p.nt;

@@ -89,11 +89,17 @@ __device__ __forceinline__ Unit decode_unit(const RingParams& p, int idx) {
   // a causal mask they carry the most key tiles. Query tiles are enumerated per
   // chunk of L rows (a shard, or a zigzag half-shard); positions grow with
   // (chunk, tile) for contiguous and zigzag, and with (tile, shard) for striped.
+  // Striped tiles are taken in blocks of 4 tile indices per shard, so that the
+  // CTAs resident at one time cover few shards: their rings then start at nearby
+  // shards and reread the same K/V tiles from L2 (at 1M tokens a kv group's K
+  // and V are four times the L2); blocks of 4 keep the order close to latest-first.
   const int key = p.X * p.nqq - 1 - r;
   int qq, c;
   if (p.layout == kStriped) {
-    qq = key / p.P;
-    c = key - qq * p.P;
+    const int QB = (p.nqq % 4 == 0) ? 4 : 1;
+    const int blk = key / (QB * p.P), rem = key - blk * QB * p.P;
+    c = rem / QB;
+    qq = blk * QB + (rem - c * QB);
   } else {
     c = key / p.nqq;
     qq = key - c * p.nqq;
