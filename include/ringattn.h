@@ -111,12 +111,13 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
 /* The full ring forward for inputs that live in HOST memory: q, k, v are read
  * from, o and lse written to, host memory (page-locked memory lets the copies
  * overlap the kernels; pageable memory also works, with the copies serialised).
- * The batch goes through the GPU one sequence at a time in two device slots of
- * the workspace: while sequence b is computed on `stream`, the inputs of b + 1
- * travel in and the outputs of b - 1 travel out on `copy_stream`, so only the
- * first sequence's inputs and the last one's outputs are not hidden behind
- * compute. Each sequence is exactly a ring_attn_fwd call (the results are the
- * same bit for bit). Work enqueued on `stream` before the call happens before
+ * The work goes through the GPU in pieces — one sequence's query heads of one
+ * kv group with that kv head — in two device slots of the workspace: while piece
+ * i is computed on `stream`, the inputs of piece i + 1 travel in and the outputs
+ * of piece i - 1 travel out on `copy_stream` (strided copies gather a group's
+ * heads), so only the first piece's inputs and the last one's outputs are not
+ * hidden behind compute. Each piece is exactly a ring_attn_fwd call on its
+ * heads (the results equal ring_attn_fwd bit for bit). Work enqueued on `stream` before the call happens before
  * any of its copies, and `stream` completes only once the outputs are in host
  * memory, so synchronising `stream` is enough. The call returns after enqueuing;
  * it creates and releases its ordering events itself. There is no counterpart in
@@ -129,8 +130,10 @@ ra_status ring_attn_fwd_host(const ra_problem* p, const void* q, const void* k, 
                              void* o, float* lse, void* workspace, size_t workspace_bytes,
                              void* stream, void* copy_stream);
 
-/* Bytes of device workspace ring_attn_fwd_host needs: two sequences' q, k, v, o,
- * lse (one if the batch is 1), each rounded up to 256 bytes. Pure host code. */
+/* Bytes of device workspace ring_attn_fwd_host needs: two pieces' q, k, v, o,
+ * lse (one piece if batch * kv_heads is 1), each rounded up to 256 bytes. A piece
+ * holds seqlen tokens of heads/kv_heads query heads and one kv head. Pure host
+ * code. */
 size_t ring_attn_fwd_host_workspace_bytes(const ra_problem* p);
 
 /* One ring step for all virtual devices at once: device u folds shard

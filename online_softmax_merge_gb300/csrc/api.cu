@@ -237,23 +237,26 @@ bool encode_ext(CUtensorMap* m, const void* base, int64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Device slot of ring_attn_fwd_host: one sequence's q, k, v, o, lse, each
-// rounded up to 256 bytes.
+// Device slot of ring_attn_fwd_host: one piece — one sequence's query heads of
+// one kv group and that kv head — as contiguous q, k, v, o, lse, each rounded up
+// to 256 bytes.
 struct HostSlot {
   size_t q, kv, o, lse, total;
 };
 HostSlot host_slot(const ra_problem* pr) {
   auto r256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t hpg = static_cast<size_t>(pr->heads / pr->kv_heads);
   HostSlot s;
-  s.q = r256(static_cast<size_t>(pr->seqlen) * pr->heads * pr->head_dim * 2);
-  s.kv = r256(static_cast<size_t>(pr->seqlen) * pr->kv_heads * pr->head_dim * 2);
+  s.q = r256(static_cast<size_t>(pr->seqlen) * hpg * pr->head_dim * 2);
+  s.kv = r256(static_cast<size_t>(pr->seqlen) * pr->head_dim * 2);
   s.o = s.q;
-  s.lse = r256(static_cast<size_t>(pr->heads) * pr->seqlen * sizeof(float));
+  s.lse = r256(hpg * pr->seqlen * sizeof(float));
   s.total = s.q + 2 * s.kv + s.o + s.lse;
   return s;
 }
 size_t fwd_host_workspace(const ra_problem* pr) {
-  return host_slot(pr).total * static_cast<size_t>(pr->batch < 2 ? pr->batch : 2);
+  const int64_t pieces = static_cast<int64_t>(pr->batch) * pr->kv_heads;
+  return host_slot(pr).total * static_cast<size_t>(pieces < 2 ? pieces : 2);
 }
 
 }  // namespace
@@ -300,20 +303,28 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
   const HostSlot hs = host_slot(pr);
-  // one sequence: a B = 1 problem with the same shapes
+  const int B = pr->batch, G = pr->kv_heads, H = pr->heads, N = pr->seqlen, D = pr->head_dim;
+  const int hpg = H / G;
+  // A piece (b, g) is the ring forward of sequence b restricted to kv group g:
+  // its query heads [g hpg, (g+1) hpg) against kv head g, a problem of its own.
   ra_problem one = *pr;
   one.batch = 1;
+  one.heads = hpg;
+  one.kv_heads = 1;
   RingParams p;
   fill_params(&one, &p);
   p.s_begin = 0;
   p.s_end = p.P;
   p.status = d->status;
-  const size_t qn = static_cast<size_t>(pr->seqlen) * pr->heads * pr->head_dim * 2;
-  const size_t kn = static_cast<size_t>(pr->seqlen) * pr->kv_heads * pr->head_dim * 2;
-  const size_t ln = static_cast<size_t>(pr->heads) * pr->seqlen * sizeof(float);
-  const int B = pr->batch;
-  // events: start (stream -> copy_stream), inputs in[b], kernel done k[b], end
-  const int n_ev = 2 + 2 * B;
+  const size_t row_q = static_cast<size_t>(H) * D * 2;      // bytes per token of q, o
+  const size_t row_kv = static_cast<size_t>(G) * D * 2;     // bytes per token of k, v
+  const size_t w_q = static_cast<size_t>(hpg) * D * 2;      // a piece's bytes per token
+  const size_t w_kv = static_cast<size_t>(D) * 2;
+  const size_t lse_piece = static_cast<size_t>(hpg) * N * sizeof(float);
+  if (static_cast<int64_t>(B) * G > (1 << 24)) return RA_ERR_UNSUPPORTED;
+  const int n_pieces = B * G;
+  // events: start (stream -> copy_stream), end, inputs in[i], kernel done k[i]
+  const int n_ev = 2 + 2 * n_pieces;
   cudaEvent_t* ev = new (std::nothrow) cudaEvent_t[n_ev];
   if (ev == nullptr) return RA_ERR_CUDA;
   int made = 0;
@@ -322,28 +333,31 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
     e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
   if (e != cudaSuccess) --made;
   cudaEvent_t ev_start = ev[0], ev_end = ev[1];
-  auto ev_in = [&](int b) { return ev[2 + b]; };
-  auto ev_k = [&](int b) { return ev[2 + B + b]; };
-  auto slot = [&](int b) { return static_cast<uint8_t*>(workspace) + (b % 2) * hs.total; };
-  auto h2d = [&](int b) -> cudaError_t {
-    uint8_t* s0 = slot(b);
-    cudaError_t r = cudaMemcpyAsync(s0, static_cast<const uint8_t*>(q) + b * qn, qn,
-                                    cudaMemcpyHostToDevice, xs);
+  auto ev_in = [&](int i) { return ev[2 + i]; };
+  auto ev_k = [&](int i) { return ev[2 + n_pieces + i]; };
+  auto slot = [&](int i) { return static_cast<uint8_t*>(workspace) + (i % 2) * hs.total; };
+  auto h2d = [&](int i) -> cudaError_t {
+    const int b = i / G, g = i % G;
+    uint8_t* s0 = slot(i);
+    const uint8_t* qs = static_cast<const uint8_t*>(q) + static_cast<size_t>(b) * N * row_q + g * w_q;
+    const uint8_t* ks = static_cast<const uint8_t*>(k) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
+    const uint8_t* vs = static_cast<const uint8_t*>(v) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
+    cudaError_t r = cudaMemcpy2DAsync(s0, w_q, qs, row_q, w_q, N, cudaMemcpyHostToDevice, xs);
     if (r == cudaSuccess)
-      r = cudaMemcpyAsync(s0 + hs.q, static_cast<const uint8_t*>(k) + b * kn, kn,
-                          cudaMemcpyHostToDevice, xs);
+      r = cudaMemcpy2DAsync(s0 + hs.q, w_kv, ks, row_kv, w_kv, N, cudaMemcpyHostToDevice, xs);
     if (r == cudaSuccess)
-      r = cudaMemcpyAsync(s0 + hs.q + hs.kv, static_cast<const uint8_t*>(v) + b * kn, kn,
-                          cudaMemcpyHostToDevice, xs);
-    if (r == cudaSuccess) r = cudaEventRecord(ev_in(b), xs);
+      r = cudaMemcpy2DAsync(s0 + hs.q + hs.kv, w_kv, vs, row_kv, w_kv, N, cudaMemcpyHostToDevice,
+                            xs);
+    if (r == cudaSuccess) r = cudaEventRecord(ev_in(i), xs);
     return r;
   };
   if (e == cudaSuccess) e = cudaEventRecord(ev_start, cs);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, ev_start, 0);
-  for (int b = 0; b < B && b < 2 && e == cudaSuccess; ++b) e = h2d(b);
-  for (int b = 0; b < B && e == cudaSuccess; ++b) {
-    uint8_t* s0 = slot(b);
-    e = cudaStreamWaitEvent(cs, ev_in(b), 0);
+  for (int i = 0; i < n_pieces && i < 2 && e == cudaSuccess; ++i) e = h2d(i);
+  for (int i = 0; i < n_pieces && e == cudaSuccess; ++i) {
+    const int b = i / G, g = i % G;
+    uint8_t* s0 = slot(i);
+    e = cudaStreamWaitEvent(cs, ev_in(i), 0);
     if (e != cudaSuccess) break;
     p.q = s0;
     p.k = s0 + hs.q;
@@ -351,15 +365,16 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
     p.o = s0 + hs.q + 2 * hs.kv;
     p.lse = reinterpret_cast<float*>(s0 + hs.q + 2 * hs.kv + hs.o);
     if ((st = run_tc(p, cs)) != RA_OK) break;
-    e = cudaEventRecord(ev_k(b), cs);
-    // outputs of b out, then (its slot free) the inputs of b + 2 in
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, ev_k(b), 0);
+    e = cudaEventRecord(ev_k(i), cs);
+    // outputs of piece i out, then (its slot free) the inputs of piece i + 2 in
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, ev_k(i), 0);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(static_cast<uint8_t*>(o) + b * qn, p.o, qn, cudaMemcpyDeviceToHost, xs);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + b * ln, p.lse, ln,
-                          cudaMemcpyDeviceToHost, xs);
-    if (e == cudaSuccess && b + 2 < B) e = h2d(b + 2);
+      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(o) + static_cast<size_t>(b) * N * row_q + g * w_q, row_q, p.o, w_q, w_q,
+                            N, cudaMemcpyDeviceToHost, xs);
+    if (e == cudaSuccess)   // lse [B, H, N]: the group's heads are consecutive rows
+      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + (static_cast<size_t>(b) * G + g) * lse_piece,
+                          p.lse, lse_piece, cudaMemcpyDeviceToHost, xs);
+    if (e == cudaSuccess && i + 2 < n_pieces) e = h2d(i + 2);
   }
   if (e == cudaSuccess && st == RA_OK) e = cudaEventRecord(ev_end, xs);
   if (e == cudaSuccess && st == RA_OK) e = cudaStreamWaitEvent(cs, ev_end, 0);

@@ -158,10 +158,12 @@ def test_bwd_argument_checks(lib):
 def test_fwd_host_workspace_and_argument_checks(lib):
     pr = _pr(batch=3, seqlen=1000, heads=4, kv_heads=2, head_dim=128, P=4)
     r = lambda x: (x + 255) // 256 * 256
-    slot = r(1000 * 4 * 128 * 2) * 2 + r(1000 * 2 * 128 * 2) * 2 + r(4 * 1000 * 4)
+    # a piece: 2 query heads (one kv group) and 1 kv head of one sequence
+    slot = r(1000 * 2 * 128 * 2) * 2 + r(1000 * 1 * 128 * 2) * 2 + r(2 * 1000 * 4)
     assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr)) == 2 * slot
-    one = _pr(batch=1, seqlen=1000, heads=4, kv_heads=2, head_dim=128, P=4)
-    assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(one)) == slot
+    one = _pr(batch=1, seqlen=1000, heads=4, kv_heads=1, head_dim=128, P=4)
+    slot1 = r(1000 * 4 * 128 * 2) * 2 + r(1000 * 1 * 128 * 2) * 2 + r(4 * 1000 * 4)
+    assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(one)) == slot1
     assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(_pr(heads=3))) == 0
     ptrs = [FAKE] * 5
     assert lib.ring_attn_fwd_host(ctypes.byref(pr), *ptrs, FAKE, 2 * slot - 1, None, None) == \

@@ -12,10 +12,12 @@ ra = pytest.importorskip("online_softmax_merge_gb300")
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 
 
-@pytest.mark.parametrize("B,layout,pinned", [(3, "contiguous", True), (1, "striped", True),
-                                             (2, "zigzag", False), (4, "striped", False)])
-def test_host_forward_equals_device_forward(B, layout, pinned):
-    w = Workload("host", B, 4 * (2 * 128 + 40), 4, 2, 128, 4, layout, True, 400 + B)
+@pytest.mark.parametrize("B,H,G,layout,pinned", [
+    (3, 4, 2, "contiguous", True), (1, 4, 2, "striped", True), (2, 4, 2, "zigzag", False),
+    (4, 4, 2, "striped", False), (2, 3, 3, "contiguous", True), (2, 4, 1, "striped", True)])
+def test_host_forward_equals_device_forward(B, H, G, layout, pinned):
+    """Pieces of one kv group each (GQA, MHA: one head per piece, MQA: all heads)."""
+    w = Workload("host", B, 4 * (2 * 128 + 40), H, G, 128, 4, layout, True, 400 + B + 10 * G)
     q, k, v = make_qkv(w)
     if pinned:
         q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
