@@ -145,49 +145,99 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- oracle
-def oracle_sample_rate(q, k, v, w, seconds: float, seed: int = 0):
-    """Run the fp64 CPU oracle on seeded random query rows of the workload until
-    `seconds` have passed; return (causal-adjusted TFLOP/s, tokens/s, rows, s)."""
-    from oracle.attention import attention_at
-    rng = np.random.default_rng(seed)
-    heads = [0, w.heads // 3, (2 * w.heads) // 3, w.heads - 1]
-    flops = 0.0
-    n_rows = 0
-    # slices converted to exact fp32 once (untimed), per (batch, kv head) in use
-    G, H = w.kv_heads, w.heads
-    prepared = {}
-    for h in heads:
-        g = (h * G) // H
-        if (0, g) not in prepared:
-            prepared[(0, g)] = (k[0:1, :, g:g + 1].float().cpu().numpy(),
-                                v[0:1, :, g:g + 1].float().cpu().numpy())
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
-        h = heads[n_rows % len(heads)]
-        g = (h * G) // H
-        kk, vv = prepared[(0, g)]
-        rows = np.sort(rng.integers(0, w.seqlen, 4))
-        qr = q[0:1, torch.as_tensor(rows, device=q.device)][:, :, h:h + 1].float().cpu().numpy()
-        attention_at(qr, rows, [0], 1, kk, vv, w.causal)
-        for t in rows:
-            flops += 4.0 * w.head_dim * ((t + 1) if w.causal else w.seqlen)
-        n_rows += len(rows)
-    dt = time.perf_counter() - t0
-    tflops = flops / dt / 1e12
-    # tokens/s of the full workload at this rate: FLOPs per token = total / (B*N)
-    tok_s = tflops * 1e12 / (w.causal_flops() / (w.batch * w.seqlen))
-    return tflops, tok_s, n_rows, dt
+# One timing worker: a child process whose BLAS/OpenMP pools were limited to one
+# thread before numpy loaded. It memory-maps the prepared K/V/Q slices, makes one
+# untimed call, waits for the common start time, then runs the oracle on seeded
+# random query rows (4 per call, cycling through the sampled heads) and reports
+# the FLOPs finished inside each window [start + i*T, start + (i+1)*T).
+_ORACLE_WORKER = r"""
+import json, os, sys, time
+import numpy as np
+from oracle.attention import attention_at
+tmp, start, T, n_win, causal, seed = (sys.argv[1], float(sys.argv[2]), float(sys.argv[3]),
+                                     int(sys.argv[4]), bool(int(sys.argv[5])), int(sys.argv[6]))
+meta = json.load(open(os.path.join(tmp, "meta.json")))
+mm = lambda name: np.load(os.path.join(tmp, name + ".npy"), mmap_mode="r")
+kv = {g: (mm(f"k{g}"), mm(f"v{g}")) for g in set(meta["groups"])}
+qs = [mm(f"q{h}") for h in meta["heads"]]
+N, d = qs[0].shape
+rng = np.random.default_rng(seed)
+def call(i, rows):
+    kk, vv = kv[meta["groups"][i]]
+    attention_at(np.asarray(qs[i][rows])[None, :, None, :], rows, [0], 1, kk, vv, causal)
+call(0, np.array([N - 1]))
+while time.time() < start:
+    time.sleep(0.005)
+out = {"flops": [0.0] * n_win, "rows": [0] * n_win}
+n = 0
+for i in range(n_win):
+    end = start + (i + 1) * T
+    while time.time() < end:
+        rows = np.sort(rng.integers(0, N, 4))
+        call(n % len(qs), rows)
+        if time.time() < end:
+            out["flops"][i] += sum(4.0 * d * ((int(t) + 1) if causal else N) for t in rows)
+            out["rows"][i] += len(rows)
+        n += 1
+print(json.dumps(out))
+"""
 
 
-def oracle_threads() -> int:
+def host_cores() -> int:
     try:
-        from threadpoolctl import threadpool_info
-        n = [x.get("num_threads", 0) for x in threadpool_info() if x.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
-    except Exception:
-        pass
-    return os.cpu_count() or 1
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rate(q, k, v, w, seconds: float, workers: int, windows: int = 1, seed: int = 0):
+    """Time the fp64 CPU oracle on seeded random query rows of batch 0 of the
+    workload (query heads 0, H/3, 2H/3, H-1): `workers` single-threaded child
+    processes run at once over `windows` common windows of `seconds` each. Work
+    finished after a window's end is not counted. Returns a list, per window, of
+    (causal-adjusted TFLOP/s summed over the workers, rows), or None on failure."""
+    import tempfile
+    H, G = w.heads, w.kv_heads
+    heads = [0, H // 3, (2 * H) // 3, H - 1]
+    groups = [(h * G) // H for h in heads]
+    with tempfile.TemporaryDirectory() as tmp:
+        for g in sorted(set(groups)):
+            np.save(os.path.join(tmp, f"k{g}.npy"), k[0:1, :, g:g + 1].float().cpu().numpy())
+            np.save(os.path.join(tmp, f"v{g}.npy"), v[0:1, :, g:g + 1].float().cpu().numpy())
+        for h in heads:
+            np.save(os.path.join(tmp, f"q{h}.npy"), q[0, :, h].float().cpu().numpy())
+        with open(os.path.join(tmp, "meta.json"), "w") as f:
+            json.dump({"heads": heads, "groups": groups}, f)
+        env = dict(os.environ)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                    "BLIS_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+            env[var] = "1"
+        env["PYTHONPATH"] = os.pathsep.join([ROOT] + [x for x in [env.get("PYTHONPATH")] if x])
+        start = time.time() + 8.0 + 0.05 * workers       # room for imports + the untimed call
+        procs = [subprocess.Popen([sys.executable, "-c", _ORACLE_WORKER, tmp, repr(start),
+                                   repr(seconds), str(windows), str(int(w.causal)),
+                                   str(seed * 1000 + i)], env=env, cwd=ROOT,
+                                  stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+                 for i in range(workers)]
+        results = []
+        limit = start + windows * seconds + 120.0
+        for pr in procs:
+            try:
+                out, _ = pr.communicate(timeout=max(1.0, limit - time.time()))
+                results.append(json.loads(out.strip().splitlines()[-1]))
+            except Exception:
+                pr.kill()
+                pr.communicate()
+                results.append(None)
+    if any(r is None for r in results):
+        return None
+    return [(sum(r["flops"][i] for r in results) / seconds / 1e12,
+             sum(r["rows"][i] for r in results)) for i in range(windows)]
+
+
+def tokens_per_s(tflops: float, w) -> float:
+    """Tokens/s of the full workload at a given causal-adjusted rate."""
+    return tflops * 1e12 / (w.causal_flops() / (w.batch * w.seqlen))
 
 
 # --------------------------------------------------------------------------- arms
@@ -197,20 +247,20 @@ def run_reference(args, w):
     if not info.is_main:
         return 0
     q, k, v = make_qkv(w, device="cpu")
-    per_step = []
-    rates = []
-    for i in range(args.warmup + args.steps):
-        tf, tok, rows, dt = oracle_sample_rate(q, k, v, w, args.ref_seconds, seed=i)
-        if i >= args.warmup:
-            per_step.append(dt)
-            rates.append((tf, tok, rows))
-    tflops = statistics.mean(r[0] for r in rates)
-    tok_s = statistics.mean(r[1] for r in rates)
-    rows = sum(r[2] for r in rates)
-    cores = oracle_threads()
+    cores = host_cores()
+    wins = oracle_rate(q, k, v, w, args.ref_seconds, cores, windows=args.warmup + args.steps)
+    if wins is None:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle timing workers failed"}))
+        return 0
+    timed = wins[args.warmup:]
+    tflops = statistics.mean(r[0] for r in timed)
+    tok_s = tokens_per_s(tflops, w)
+    rows = sum(r[1] for r in timed)
+    per_step = [args.ref_seconds] * len(timed)
     sample = (f"{rows} seeded random query rows of batch 0, heads 0/{w.heads // 3}/"
-              f"{(2 * w.heads) // 3}/{w.heads - 1}, ~{args.ref_seconds:.0f} s per step, "
-              "exact fp64 rows; FLOPs counted causal-adjusted")
+              f"{(2 * w.heads) // 3}/{w.heads - 1}, exact fp64, {cores} single-threaded "
+              f"worker processes, one {args.ref_seconds:.0f} s window per step; FLOPs "
+              "counted causal-adjusted")
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -421,11 +471,21 @@ def run_ours(args, w):
     # ---- the oracle on the host cores (rank 0 only)
     cpu = None
     if info.is_main and not args.no_cpu_baseline:
-        tf, tok, rows, dt = oracle_sample_rate(q, k, v, w, args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
-               "sample": f"{rows} seeded random query rows (batch 0, 4 heads) of the same "
-                         f"workload, exact fp64, {dt:.1f} s; FLOPs counted causal-adjusted",
-               "tokens_per_s": tok}
+        cores = host_cores()
+        allc = oracle_rate(q, k, v, w, args.cpu_seconds, cores)
+        one = oracle_rate(q, k, v, w, args.one_core_seconds, 1, seed=1)
+        if allc is not None:
+            tf, rows = allc[0]
+            cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{rows} seeded random query rows (batch 0, 4 heads) of the same "
+                             f"workload, exact fp64, {cores} single-threaded worker processes "
+                             f"over one {args.cpu_seconds:.0f} s window; FLOPs counted "
+                             "causal-adjusted",
+                   "tokens_per_s": tokens_per_s(tf, w)}
+            if one is not None:
+                cpu["one_core"] = {"value": one[0][0], "unit": "TFLOP/s", "cores": 1,
+                                   "sample": f"{one[0][1]} rows, one worker process, "
+                                             f"{args.one_core_seconds:.0f} s"}
 
     if info.is_main:
         line = {
@@ -463,6 +523,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--one-core-seconds", type=float, default=6.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-merge", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
