@@ -11,7 +11,11 @@ with inputs resident in HBM. Also measured in the same run:
     d=128 problem (HBM-bound), as GB/s against the measured copy bandwidth;
   * decode: ring_attn_decode of one query token per sequence against the same
     KV cache (per-shard partials + merge; HBM-bound), as GB/s;
-  * cpu_baseline: the fp64 CPU oracle on a bounded sample of query rows.
+  * step_path: the same forward composed from P ring_attn_step calls (running state in
+    HBM) and ring_attn_finalize;
+  * bwd: the backward ring (ring_attn_bwd) on the same workload;
+  * cpu_baseline: the fp64 CPU oracle on a bounded sample of query rows, one
+    single-threaded worker process per host core, plus a one-core figure.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--impl ours|reference]
 
@@ -441,6 +445,34 @@ def run_ours(args, w):
                               f"P={w.P} {w.layout}); partials per (shard, 4096-key chunk) + merge"}
         del qd, ws, od, ld
 
+    # ---- the same forward composed from the step API: P ring_attn_step calls with the
+    # running (m, z, y) in HBM, then ring_attn_finalize
+    step_path = None
+    if not args.no_step:
+        state = ra.empty_state(q)
+        so = torch.empty_like(o)
+        sl = torch.empty_like(lse)
+
+        def composed():
+            for s in range(w.P):
+                ra.step(q, k, v, w.P, s, state, s == 0, w.layout, w.causal)
+            ra.finalize(state, w.P, w.layout, w.causal, out=so, lse=sl)
+
+        composed()
+        torch.cuda.synchronize(dev)
+        ms = time_launches(composed, max(2, min(args.steps, 3)), stream)
+        if ra.last_error(dev) != 0:
+            raise RuntimeError("device-side wait timed out in the step path")
+        tf = flops_step / (statistics.mean(ms) * 1e-3) / 1e12
+        step_path = {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": tf / peak_tf, "ms": statistics.mean(ms),
+                     "launches_per_call": w.P + 1,
+                     "max_abs_diff_vs_fused": {"o": float((so.float() - o.float()).abs().max()),
+                                               "lse": float((sl - lse).abs().max())},
+                     "workload": f"the {w.name} forward as {w.P} ring_attn_step calls (state "
+                                 "m, z, y fp32 in HBM) + ring_attn_finalize"}
+        del state, so, sl
+
     # ---- backward ring on the same workload, from this forward's O and LSE
     bwd = None
     if not args.no_bwd:
@@ -502,6 +534,7 @@ def run_ours(args, w):
             "merge_roofline": merge,
             "decode_roofline": decode,
             "bwd_roofline": bwd,
+            "step_path": step_path,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -528,6 +561,7 @@ def main():
     ap.add_argument("--no-merge", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-step", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

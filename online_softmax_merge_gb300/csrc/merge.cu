@@ -8,11 +8,12 @@
 // O = sum_p e^{LSE_p - LSE} O_p. Finalize — "Ring Attention" (aarnphm.xyz):
 // O = y / z; LSE = m + ln z.
 //
-// Layout: a block owns 32 consecutive tokens of one (batch, head). Its first warp
-// reduces the 32 rows' log-sum-exps (lane = token, coalesced over tokens for each
-// part); then each warp streams whole rows: a row of d fp32 is one coalesced
-// 16-byte-per-lane (d = 128) or 8-byte-per-lane (d = 64) load per part, several
-// parts in flight per lane.
+// Layout: a block owns 32 consecutive tokens of one (batch, head); warp w takes
+// tokens w, w + 8, w + 16, w + 24. A warp first reduces the log-sum-exps of its own
+// four tokens (eight lanes per token, each over every eighth part, combined by
+// shuffles; no block barrier), then streams whole rows: a row of d fp32 is one
+// coalesced 16-byte-per-lane (d = 128) or 8-byte-per-lane (d = 64) load per part,
+// four parts in flight per lane.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -22,7 +23,7 @@ namespace ra {
 namespace {
 
 constexpr int kTok = 32;      // tokens per block
-constexpr int kWarps = 8;     // 4 tokens per warp
+constexpr int kWarps = 8;     // 4 tokens per warp (kTok = 4 * kWarps)
 
 template <int D>
 struct Vec;
@@ -53,7 +54,6 @@ merge_kernel(int n, int B, int N, int H, const float* __restrict__ o_parts,
              float* __restrict__ lse) {
   using V = Vec<D>;
   constexpr int kN = V::kN;
-  __shared__ float s_lse[kTok];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kTok;
   const int head = blockIdx.y;
@@ -62,32 +62,52 @@ merge_kernel(int n, int B, int N, int H, const float* __restrict__ o_parts,
   const size_t part_o = static_cast<size_t>(B) * N * H * D;
   const size_t lrow = (static_cast<size_t>(bat) * H + head) * N;    // [B,H,N] row base
 
-  if (warp == 0) {
-    const int t = t0 + lane;
+  // Each warp reduces the log-sum-exps of its own four tokens (tt = warp + 8 j):
+  // lanes 8j .. 8j+7 take parts pl, pl + 8, ... of token slot j and combine by shuffles.
+  float Lw;
+  {
+    const int slot = lane >> 3, pl = lane & 7;
+    const int t = t0 + warp + kWarps * slot;
     float M = -INFINITY, acc = 0.f;
     if (t < N) {
-      // online log-sum-exp over the parts
-      for (int q = 0; q < n; ++q) {
-        const float l = __ldcs(lse_parts + q * part_lse + lrow + t);
-        if (l == -INFINITY) continue;
-        if (l > M) {
-          acc = acc * expf(M - l) + 1.f;
-          M = l;
-        } else {
-          acc += expf(l - M);
+      for (int q0 = pl; q0 < n; q0 += 32) {
+        float lv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          lv[k] = (q0 + 8 * k < n) ? __ldg(lse_parts + (q0 + 8 * k) * part_lse + lrow + t)
+                                   : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float l = lv[k];
+          if (l == -INFINITY) continue;
+          if (l > M) {
+            acc = acc * expf(M - l) + 1.f;
+            M = l;
+          } else {
+            acc += expf(l - M);
+          }
         }
       }
     }
-    const float L = (M == -INFINITY) ? -INFINITY : M + logf(acc);
-    s_lse[lane] = L;
-    if (t < N) lse[lrow + t] = L;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+      const float ao = __shfl_xor_sync(0xffffffffu, acc, off);
+      const float Mn = fmaxf(M, Mo);
+      float s = 0.f;
+      if (M != -INFINITY) s += acc * expf(M - Mn);
+      if (Mo != -INFINITY) s += ao * expf(Mo - Mn);
+      M = Mn;
+      acc = s;
+    }
+    Lw = (M == -INFINITY) ? -INFINITY : M + logf(acc);
+    if (pl == 0 && t < N) lse[lrow + t] = Lw;
   }
-  __syncthreads();
-
-  for (int tt = warp; tt < kTok; tt += kWarps) {
-    const int t = t0 + tt;
+#pragma unroll 1
+  for (int j = 0; j < 4; ++j) {
+    const float L = __shfl_sync(0xffffffffu, Lw, 8 * j);   // all lanes: t is warp-uniform
+    const int t = t0 + warp + kWarps * j;
     if (t >= N) break;
-    const float L = s_lse[tt];
     const size_t orow = ((static_cast<size_t>(bat) * N + t) * H + head) * D;
     float acc[kN];
 #pragma unroll
