@@ -151,15 +151,16 @@ class ClockSampler:
 # --------------------------------------------------------------------------- oracle
 # One timing worker: a child process whose BLAS/OpenMP pools were limited to one
 # thread before numpy loaded. It memory-maps the prepared K/V/Q slices, makes one
-# untimed call, waits for the common start time, then runs the oracle on seeded
+# untimed call per head, prints "ready", waits for the parent to publish the common
+# start time (written once every worker is ready), then runs the oracle on seeded
 # random query rows (4 per call, cycling through the sampled heads) and reports
 # the FLOPs finished inside each window [start + i*T, start + (i+1)*T).
 _ORACLE_WORKER = r"""
 import json, os, sys, time
 import numpy as np
 from oracle.attention import attention_at
-tmp, start, T, n_win, causal, seed = (sys.argv[1], float(sys.argv[2]), float(sys.argv[3]),
-                                     int(sys.argv[4]), bool(int(sys.argv[5])), int(sys.argv[6]))
+tmp, T, n_win, causal, seed = (sys.argv[1], float(sys.argv[2]), int(sys.argv[3]),
+                               bool(int(sys.argv[4])), int(sys.argv[5]))
 meta = json.load(open(os.path.join(tmp, "meta.json")))
 mm = lambda name: np.load(os.path.join(tmp, name + ".npy"), mmap_mode="r")
 kv = {g: (mm(f"k{g}"), mm(f"v{g}")) for g in set(meta["groups"])}
@@ -169,9 +170,15 @@ rng = np.random.default_rng(seed)
 def call(i, rows):
     kk, vv = kv[meta["groups"][i]]
     attention_at(np.asarray(qs[i][rows])[None, :, None, :], rows, [0], 1, kk, vv, causal)
-call(0, np.array([N - 1]))
-while time.time() < start:
+for i in range(len(qs)):
+    call(i, np.array([N - 1]))
+print("ready", flush=True)
+start_file, give_up = os.path.join(tmp, "start"), time.time() + 600.0
+while not os.path.exists(start_file) and time.time() < give_up:
     time.sleep(0.005)
+start = float(open(start_file).read())
+while time.time() < start:
+    time.sleep(0.001)
 out = {"flops": [0.0] * n_win, "rows": [0] * n_win}
 n = 0
 for i in range(n_win):
@@ -183,8 +190,22 @@ for i in range(n_win):
             out["flops"][i] += sum(4.0 * d * ((int(t) + 1) if causal else N) for t in rows)
             out["rows"][i] += len(rows)
         n += 1
-print(json.dumps(out))
+print(json.dumps(out), flush=True)
 """
+
+def wait_ready(procs, timeout: float) -> bool:
+    """Read the "ready" line of every worker (select on their pipes, bounded)."""
+    import select
+    pending = {pr.stdout.fileno(): pr for pr in procs}
+    end = time.time() + timeout
+    while pending and time.time() < end:
+        fds, _, _ = select.select(list(pending), [], [], 1.0)
+        for fd in fds:
+            line = pending[fd].stdout.readline()
+            if line.strip() != "ready":
+                return False
+            del pending[fd]
+    return not pending
 
 
 def host_cores() -> int:
@@ -217,18 +238,22 @@ def oracle_rate(q, k, v, w, seconds: float, workers: int, windows: int = 1, seed
                     "BLIS_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
             env[var] = "1"
         env["PYTHONPATH"] = os.pathsep.join([ROOT] + [x for x in [env.get("PYTHONPATH")] if x])
-        start = time.time() + 8.0 + 0.05 * workers       # room for imports + the untimed call
-        procs = [subprocess.Popen([sys.executable, "-c", _ORACLE_WORKER, tmp, repr(start),
-                                   repr(seconds), str(windows), str(int(w.causal)),
-                                   str(seed * 1000 + i)], env=env, cwd=ROOT,
-                                  stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+        procs = [subprocess.Popen([sys.executable, "-c", _ORACLE_WORKER, tmp, repr(seconds),
+                                   str(windows), str(int(w.causal)), str(seed * 1000 + i)],
+                                  env=env, cwd=ROOT, stdout=subprocess.PIPE,
+                                  stderr=subprocess.DEVNULL, text=True)
                  for i in range(workers)]
+        ok = wait_ready(procs, timeout=600.0)
+        start = time.time() + 0.2
+        with open(os.path.join(tmp, "start.part"), "w") as f:
+            f.write(repr(start if ok else 0.0))
+        os.replace(os.path.join(tmp, "start.part"), os.path.join(tmp, "start"))
         results = []
         limit = start + windows * seconds + 120.0
         for pr in procs:
             try:
                 out, _ = pr.communicate(timeout=max(1.0, limit - time.time()))
-                results.append(json.loads(out.strip().splitlines()[-1]))
+                results.append(json.loads(out.strip().splitlines()[-1]) if ok else None)
             except Exception:
                 pr.kill()
                 pr.communicate()
