@@ -117,10 +117,12 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
  * of piece i - 1 travel out on `copy_stream` (strided copies gather a group's
  * heads), so only the first piece's inputs and the last one's outputs are not
  * hidden behind compute. Each piece is exactly a ring_attn_fwd call on its
- * heads (the results equal ring_attn_fwd bit for bit). Work enqueued on `stream` before the call happens before
- * any of its copies, and `stream` completes only once the outputs are in host
- * memory, so synchronising `stream` is enough. The call returns after enqueuing;
- * it creates and releases its ordering events itself. There is no counterpart in
+ * heads (the results equal ring_attn_fwd bit for bit). Work enqueued on `stream`
+ * before the call happens before any of its copies, and `stream` completes only
+ * once the outputs are in host memory, so synchronising `stream` is enough; that
+ * holds after an error returned midway too (`stream` still waits for every copy
+ * already queued) before the workspace or host buffers are reused. The call
+ * returns after enqueuing; it creates and releases its ordering events itself. There is no counterpart in
  * the pages: this is an interface choice of this library (host-resident inputs,
  * e.g. in the CPU memory of a Grace host).
  * q, k, v, o, lse: host pointers in the shapes of ring_attn_fwd. workspace:

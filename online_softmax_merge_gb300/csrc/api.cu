@@ -376,8 +376,13 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
                           p.lse, lse_piece, cudaMemcpyDeviceToHost, xs);
     if (e == cudaSuccess && i + 2 < n_pieces) e = h2d(i + 2);
   }
-  if (e == cudaSuccess && st == RA_OK) e = cudaEventRecord(ev_end, xs);
-  if (e == cudaSuccess && st == RA_OK) e = cudaStreamWaitEvent(cs, ev_end, 0);
+  // Join the copy stream back into `stream`, also after an error: copies already queued
+  // may still write the workspace, and the caller orders its reuse on `stream`.
+  if (made == n_ev) {
+    const cudaError_t j = cudaEventRecord(ev_end, xs);
+    const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(cs, ev_end, 0) : j;
+    if (e == cudaSuccess) e = w;
+  }
   for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);   // released once they complete
   delete[] ev;
   if (st != RA_OK) return st;
