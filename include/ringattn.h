@@ -63,7 +63,8 @@ extern "C" {
 typedef enum {
   RA_OK = 0,
   RA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, N % P != 0, H % G != 0, misaligned */
-  RA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, or no sm_103a device */
+  RA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, no sm_103a device, or a size past a
+                               launch limit (e.g. batch x heads x P x query tiles >= 2^31) */
   RA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
   RA_ERR_TIMEOUT = 4        /* a device-side wait ran out (read via ring_attn_last_error) */
 } ra_status;

@@ -81,6 +81,13 @@ ra_status check_problem(const ra_problem* pr) {
   // tensor-map extents (< 2^32 per dimension)
   const double elems = static_cast<double>(pr->batch) * pr->seqlen * pr->heads * pr->head_dim;
   if (elems > 9.0e15) return RA_ERR_INVALID_ARG;
+  // the forward launches at most one CTA per (batch, query head, chunk, 128-row
+  // query tile); its 1-D grid must stay below 2^31
+  const int64_t X = pr->layout == RA_LAYOUT_ZIGZAG ? 2 * pr->P : pr->P;
+  const int64_t L = pr->seqlen / X;
+  if (static_cast<int64_t>(pr->batch) * pr->heads * X * ((L + 127) / 128) >=
+      (static_cast<int64_t>(1) << 31))
+    return RA_ERR_UNSUPPORTED;
   return RA_OK;
 }
 

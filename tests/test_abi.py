@@ -64,6 +64,9 @@ FAKE = ctypes.c_void_p(0x10000)      # aligned, never dereferenced: checks fail 
     (dict(scale=-1.0), _lib.RA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), _lib.RA_ERR_INVALID_ARG),
     (dict(head_dim=96), _lib.RA_ERR_UNSUPPORTED),
+    # 2^31 forward CTAs (batch x heads x shards x query tiles): past the 1-D grid
+    (dict(batch=1024, seqlen=1 << 20, heads=256, kv_heads=256, head_dim=64, P=8),
+     _lib.RA_ERR_UNSUPPORTED),
 ])
 def test_fwd_rejects_bad_problems_before_any_launch(lib, bad, code):
     pr = _pr(**bad)
