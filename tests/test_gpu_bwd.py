@@ -200,3 +200,24 @@ def test_bwd_c5_one_million_tokens_sampled():
     rows = sorted({0, w.P, N - 1} | set(rng.integers(0, N, 3).tolist()))
     keys = [N - 1, N - 65, N - 200]
     _sampled(w, rows, keys, groups=[7])
+
+
+@pytest.mark.parametrize("scale,layout,d", [(0.05, "contiguous", 128), (0.3, "striped", 128),
+                                            (0.5, "zigzag", 64)])
+def test_fwd_and_bwd_with_explicit_scale(scale, layout, d):
+    """A score scale other than 1/sqrt(d): the forward's O and LSE and all three
+    gradients follow the oracle run with the same scale (the backward folds
+    -LSE/scale into its products, so a wrong scale anywhere shows here)."""
+    w = Workload("scale", 1, 4 * (2 * 128 + 40), 4, 2, d, 4, layout, True, 217)
+    q, k, v, do = _inputs(w)
+    o, lse = ra.fwd(q, k, v, w.P, w.layout, w.causal, scale)
+    dq, dk, dv = ra.bwd(q, k, v, o, lse, do, w.P, w.layout, w.causal, scale)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    hq, hk, hv, hdo = (host32(t).astype(np.float64) for t in (q, k, v, do))
+    O, LSE = OA.dense_attention(hq, hk, hv, w.causal, scale=scale)
+    assert np.abs(host32(o) - O).max() <= 1e-2
+    assert np.abs(host32(lse) - LSE).max() <= 1e-3
+    ref = OB.attention_grads(hq, hk, hv, hdo, w.causal, scale=scale)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        assert_close(host32(got), r, name)

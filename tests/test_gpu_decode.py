@@ -15,13 +15,14 @@ ra = pytest.importorskip("online_softmax_merge_gb300")
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 
 
-def _check(q, k, v, P, q_pos0, layout, causal):
-    o, lse = ra.decode(q, k, v, P, q_pos0, layout, causal)
+def _check(q, k, v, P, q_pos0, layout, causal, scale=0.0):
+    o, lse = ra.decode(q, k, v, P, q_pos0, layout, causal, scale)
     torch.cuda.synchronize()
     assert ra.last_error(DEV) == 0
     n_q, H = q.shape[1], q.shape[2]
     rows = np.arange(q_pos0, q_pos0 + n_q)
-    O_ref, L_ref = attention_at(host32(q), rows, list(range(H)), H, host32(k), host32(v), causal)
+    O_ref, L_ref = attention_at(host32(q), rows, list(range(H)), H, host32(k), host32(v), causal,
+                                scale=scale if scale > 0 else None)
     eo = float(np.abs(host32(o) - O_ref).max())
     el = float(np.abs(host32(lse) - L_ref).max())
     return eo, el
@@ -53,6 +54,16 @@ def test_decode_matches_oracle(case):
     g = torch.Generator().manual_seed(17)
     q = torch.randn((B, n_q, H, d), generator=g).to(torch.bfloat16)
     eo, el = _check(q.to(DEV), k.to(DEV), v.to(DEV), P, q_pos0, layout, causal)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+
+
+@pytest.mark.parametrize("scale", [0.04, 0.5])
+def test_decode_with_explicit_scale(scale):
+    w = Workload("decs", 1, 4 * 700, 8, 2, 128, 4, "striped", True, seed=340)
+    _, k, v = make_qkv(w)
+    g = torch.Generator().manual_seed(18)
+    q = torch.randn((1, 2, 8, 128), generator=g).to(torch.bfloat16)
+    eo, el = _check(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.seqlen - 2, w.layout, True, scale)
     assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
 
 

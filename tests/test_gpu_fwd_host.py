@@ -1,6 +1,7 @@
 """ring_attn_fwd_host: the ring forward for inputs in host memory, pipelined one
-sequence at a time through two device slots. Each sequence is a ring_attn_fwd call,
-so the results must equal the device path bit for bit."""
+(sequence, kv group) piece at a time through two device slots. Each piece is a
+ring_attn_fwd call on its heads, so the results must equal the device path bit for
+bit."""
 import pytest
 import torch
 
@@ -45,6 +46,17 @@ def test_host_forward_after_prior_work_on_the_stream(same_stream):
                            copy_stream=cur if same_stream else None)
     torch.cuda.synchronize()
     o_d, l_d = ra.fwd(q_dev, k.to(DEV), v.to(DEV), w.P, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())
+
+
+def test_host_forward_with_explicit_scale():
+    w = Workload("hosts", 2, 4 * 200, 4, 2, 64, 4, "striped", True, 420)
+    q, k, v = (t.pin_memory() for t in make_qkv(w))
+    o_h, l_h = ra.fwd_host(q, k, v, w.P, w.layout, w.causal, scale=0.3, device=DEV)
+    torch.cuda.synchronize()
+    o_d, l_d = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal, 0.3)
     torch.cuda.synchronize()
     assert torch.equal(o_h, o_d.cpu())
     assert torch.equal(l_h, l_d.cpu())
