@@ -1,8 +1,8 @@
-"""Seeded random problem shapes: the forward, the backward and pass-Q decode against
-the fp64 oracle over every layout, both head sizes, GQA/MHA/MQA head groupings,
-shard lengths that are not multiples of the 128-row tile, P = 1 and one-token
-shards. Each shape is drawn from a fixed seed, so a failure names a reproducible
-case."""
+"""Seeded random problem shapes: the forward, the backward, pass-Q decode and the
+composed step path against the fp64 oracle over every layout, both head sizes,
+GQA/MHA/MQA head groupings, shard lengths that are not multiples of the 128-row
+tile, P = 1 and one-token shards. Each shape is drawn from a fixed seed, so a
+failure names a reproducible case."""
 import numpy as np
 import pytest
 import torch
@@ -92,3 +92,18 @@ def test_fuzz_decode(w):
                                 host32(v), w.causal)
     assert float(np.abs(host32(o) - O_ref).max()) <= TOL_O
     assert float(np.abs(host32(lse) - L_ref).max()) <= TOL_LSE
+
+
+@pytest.mark.parametrize("w", CASES[1::4], ids=IDS[1::4])
+def test_fuzz_step_path(w):
+    """P ring_attn_step calls (state in HBM) and ring_attn_finalize: the same O and
+    LSE as the oracle."""
+    q, k, v = (t.to(DEV) for t in make_qkv(w))
+    state = ra.empty_state(q)
+    for s in range(w.P):
+        ra.step(q, k, v, w.P, s, state, s == 0, w.layout, w.causal)
+    o, lse = ra.finalize(state, w.P, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    eo, el = compare_full(o, lse, q, k, v, w.causal)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
