@@ -44,6 +44,12 @@
  *  concurrent calls on different streams are safe when their output buffers
  *  (and workspaces) do not overlap.
  *
+ *  CUDA graphs: after a device's first eager call of an entry point (which sets
+ *  the kernels' shared-memory limits and reads the device's facts), the calls
+ *  that launch kernels on `stream` only — every one but ring_attn_fwd_host and
+ *  ring_attn_last_error — may be captured into a graph; a replay computes what
+ *  the eager call would on the buffers' contents at replay time.
+ *
  *  Errors: argument errors are returned synchronously before any launch and
  *  nothing is written. RA_ERR_CUDA means a CUDA call (launch or tensor-map
  *  encode) failed. A device-side wait that exceeds its time limit makes the
