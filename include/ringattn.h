@@ -72,7 +72,9 @@ typedef enum {
   RA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, no sm_103a device, or a size past a
                                launch limit (e.g. batch x heads x P x query tiles >= 2^31) */
   RA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
-  RA_ERR_TIMEOUT = 4        /* a device-side wait ran out (read via ring_attn_last_error) */
+  RA_ERR_TIMEOUT = 4,       /* a device-side wait ran out (read via ring_attn_last_error) */
+  RA_ERR_BOUNDS = 5         /* debug builds only (RA_DEBUG): a kernel's index check failed and
+                               the access was skipped (read via ring_attn_last_error) */
 } ra_status;
 
 /* Shard layouts ("Part 4: Ring Attention" §4.3.1 for contiguous; "Ring Attention"
@@ -294,6 +296,21 @@ ra_status ring_attn_last_error(int32_t* device_code);
  * records RA_ERR_TIMEOUT in the status word and returns. Lets a test see the
  * timeout path without a hang. 0 < limit_ns <= 10^9. */
 ra_status ring_attn_selftest_timeout(uint64_t limit_ns, void* stream);
+
+/* 1 if this library was built with the kernels' index checks (RA_DEBUG), else 0.
+ * In such a debug build every raw global load or store (one that is not a TMA copy)
+ * of the ring, step, backward and decode kernels first checks its index range
+ * against its buffer; a failed check records RA_ERR_BOUNDS in the status word and
+ * skips the access. (The merge, finalize and index-map kernels address memory only
+ * through their launch coordinates under explicit guards and carry no checks.)
+ * Results are otherwise those of the release build. No counterpart in the pages. */
+int32_t ring_attn_debug_checks(void);
+
+/* Launches one thread that checks the index range [4, 5) against a 4-element
+ * extent without accessing memory: a debug build records RA_ERR_BOUNDS in the
+ * status word, a release build records nothing. Lets a test see the check path
+ * fire without a faulty kernel. */
+ra_status ring_attn_selftest_bounds(void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* ra_status_str(ra_status s);

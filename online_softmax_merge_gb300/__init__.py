@@ -17,11 +17,12 @@ from typing import Optional, Tuple
 import torch
 
 from . import _lib
-from ._lib import (LAYOUTS, RA_ERR_CUDA, RA_ERR_INVALID_ARG, RA_ERR_TIMEOUT,  # noqa: F401
-                   RA_ERR_UNSUPPORTED, RA_OK, TILE, RingAttnError, check, load)
+from ._lib import (LAYOUTS, RA_ERR_BOUNDS, RA_ERR_CUDA, RA_ERR_INVALID_ARG,  # noqa: F401
+                   RA_ERR_TIMEOUT, RA_ERR_UNSUPPORTED, RA_OK, TILE, RingAttnError, check, load)
 
 __all__ = ["fwd", "fwd_host", "fwd_host_workspace_bytes", "bwd", "bwd_workspace_bytes", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
-           "tile_classes", "mask", "last_error", "selftest_timeout", "problem", "RingAttnError",
+           "tile_classes", "mask", "last_error", "selftest_timeout", "selftest_bounds",
+           "debug_checks", "problem", "RingAttnError",
            "empty_state", "LAYOUTS", "TILE"]
 
 
@@ -371,6 +372,20 @@ def last_error(device="cuda") -> int:
     with torch.cuda.device(torch.device(device)):
         check("ring_attn_last_error", lib.ring_attn_last_error(ctypes.byref(code)))
     return int(code.value)
+
+
+def debug_checks() -> bool:
+    """True if the loaded library is the debug build (kernels check their indices)."""
+    return bool(load().ring_attn_debug_checks())
+
+
+def selftest_bounds(device="cuda") -> None:
+    """Launch the index-check self test: a debug build records RA_ERR_BOUNDS, a
+    release build nothing (no memory is accessed either way)."""
+    lib = load()
+    device = torch.device(device)
+    with torch.cuda.device(device):
+        check("ring_attn_selftest_bounds", lib.ring_attn_selftest_bounds(_stream(device)))
 
 
 def selftest_timeout(limit_ns: int, device="cuda") -> None:

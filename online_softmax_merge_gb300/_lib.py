@@ -1,6 +1,8 @@
 """ctypes loader for libringattn.so (the C ABI in include/ringattn.h).
 
 Loading fails loudly when the library has not been built: there is no fallback.
+With RA_DEBUG=1 in the environment the debug build libringattn_debug.so (the same
+kernels with index checks) is loaded instead.
 """
 from __future__ import annotations
 
@@ -8,11 +10,12 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libringattn.so")
+LIB_PATH = os.path.join(HERE, "libringattn_debug.so" if os.environ.get("RA_DEBUG") == "1"
+                        else "libringattn.so")
 
-RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT = range(5)
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_ERR_BOUNDS = range(6)
 STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
-                4: "RA_ERR_TIMEOUT"}
+                4: "RA_ERR_TIMEOUT", 5: "RA_ERR_BOUNDS"}
 LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
 TILE = 128
 
@@ -46,6 +49,8 @@ SIGNATURES = {
     "ring_attn_mask": (_i32, [_PP, _i32, _i32, _vp, _vp]),
     "ring_attn_last_error": (_i32, [ctypes.POINTER(ctypes.c_int32)]),
     "ring_attn_selftest_timeout": (_i32, [_u64, _vp]),
+    "ring_attn_selftest_bounds": (_i32, [_vp]),
+    "ring_attn_debug_checks": (_i32, []),
     "ra_status_str": (ctypes.c_char_p, [_i32]),
     "ring_attn_version": (_i32, []),
 }
@@ -68,7 +73,7 @@ def load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
-            "(or python online_softmax_merge_gb300/build.py) first")
+            "(or python online_softmax_merge_gb300/build.py [--debug]) first")
     lib = ctypes.CDLL(LIB_PATH)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)

@@ -2,7 +2,10 @@
 
 Each .cu file under csrc/ is compiled to an object in parallel, then linked
 into online_softmax_merge_gb300/libringattn.so against the shared CUDA runtime.
-Rebuilds only when a source or header is newer than the library.
+Rebuilds only when a source or header is newer than the library. With --debug
+(build(debug=True)) the same sources become libringattn_debug.so with the
+kernels' index checks compiled in (-DRA_DEBUG); the binding loads that library
+instead when the environment sets RA_DEBUG=1.
 """
 from __future__ import annotations
 
@@ -18,6 +21,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libringattn.so")
+# the same sources with the kernels' index checks compiled in (-DRA_DEBUG)
+DEBUG_BUILD_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(HERE, "libringattn_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -41,24 +47,29 @@ def _deps():
             glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link; returns the library path."""
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags=None,
+          debug: bool = False) -> str:
+    """Compile and link; returns the library path. debug=True builds
+    libringattn_debug.so with the kernels' index checks (-DRA_DEBUG)."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                    "-I", INCLUDE, "-I", CSRC] + list(extra_flags or [])
+                    "-I", INCLUDE, "-I", CSRC] + (["-DRA_DEBUG"] if debug else []) + list(
+                        extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, "-c", src, "-o", obj] + flags
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,16 +80,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, "-shared", "-cudart", "shared", "-o", tmp] + ARCH + objs + [
         "-Xlinker", "-rpath," + cuda_lib_dir(nvcc)]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -668,10 +668,20 @@ const char* ra_status_str(ra_status s) {
     case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
     case RA_ERR_CUDA: return "RA_ERR_CUDA";
     case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+    case RA_ERR_BOUNDS: return "RA_ERR_BOUNDS";
   }
   return "RA_ERR_UNKNOWN";
 }
 
 int32_t ring_attn_version(void) { return 100; }
+
+int32_t ring_attn_debug_checks(void) { return kDebugChecks ? 1 : 0; }
+
+ra_status ring_attn_selftest_bounds(void* stream) {
+  DevInfo* d = nullptr;
+  ra_status st = current_device(&d);
+  if (st != RA_OK) return st;
+  return launch_result(launch_selftest_bounds(d->status, static_cast<cudaStream_t>(stream)));
+}
 
 }  // extern "C"

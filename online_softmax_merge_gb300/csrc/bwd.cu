@@ -193,6 +193,15 @@ __device__ __forceinline__ const float* stats_tile(const BwdParams& p, int bat, 
   return p.ws + ((((static_cast<size_t>(bat) * p.H + h) * p.X + chunk) * p.nt + tile) << 8);
 }
 
+// Workspace extents: tiles x 256 statistics floats, then (2 tiles + 1) extension
+// tiles of 128 rows x 16 bf16.
+__device__ __forceinline__ size_t stats_elems(const BwdParams& p) {
+  return static_cast<size_t>(p.tiles) << 8;
+}
+__device__ __forceinline__ size_t ext_elems(const BwdParams& p) {
+  return (2 * static_cast<size_t>(p.tiles) + 1) << 11;
+}
+
 // --------------------------------------------------------------------------- prep
 // One row per TPR = D/8 threads (16 bytes of O and of dO each); warps advance
 // together so the shuffles always see whole groups.
@@ -219,9 +228,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
     const bool valid = in && ii < p.L;
     float dsum = 0.f;
     float l2 = INFINITY;
-    if (valid) {
-      const int pos = p.layout == kStriped ? ii * p.P + c : c * p.L + ii;
-      const size_t off = ((static_cast<size_t>(bat) * p.N + pos) * p.H + h) * D + sub * 8;
+    const int pos = p.layout == kStriped ? ii * p.P + c : c * p.L + ii;
+    const size_t off = ((static_cast<size_t>(bat) * p.N + pos) * p.H + h) * D + sub * 8;
+    const size_t li = (static_cast<size_t>(bat) * p.H + h) * p.N + pos;
+    if (valid && in_bounds(off, 8, q_elems(p), p.status) &&
+        in_bounds(li, 1, row_elems(p), p.status)) {
       const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + off);
       const uint4 b =
           *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + off);
@@ -234,13 +245,16 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
         dsum = fmaf(fa.x, fb.x, dsum);
         dsum = fmaf(fa.y, fb.y, dsum);
       }
-      const float l = p.lse[(static_cast<size_t>(bat) * p.H + h) * p.N + pos];
+      const float l = p.lse[li];
       l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;   // a row with no key contributes 0
     }
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-    if (in && sub == 0) {
-      const size_t tile = ((static_cast<size_t>(bat) * p.H + h) * p.X + c) * p.nt + (ii >> 7);
+    const size_t tile = ((static_cast<size_t>(bat) * p.H + h) * p.X + c) * p.nt + (ii >> 7);
+    const size_t r7 = ii & 127;
+    if (in && sub == 0 && in_bounds((tile << 8) + r7, 129, stats_elems(p), p.status) &&
+        in_bounds(((tile << 7) + r7) * 16, 16, ext_elems(p), p.status) &&
+        in_bounds((((p.tiles + tile) << 7) + r7) * 16, 16, ext_elems(p), p.status)) {
       float* dst = p.ws + (tile << 8) + (ii & 127);
       dst[0] = l2;
       dst[128] = dsum;
@@ -269,7 +283,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
     }
   }
   // key-side extension tile: ones in columns 0-2 of all 128 rows
-  if (blockIdx.x == 0 && threadIdx.x < 128) {
+  if (blockIdx.x == 0 && threadIdx.x < 128 &&
+      in_bounds(((2 * static_cast<size_t>(p.tiles)) << 11) + threadIdx.x * 16, 16, ext_elems(p),
+                p.status)) {
     const uint32_t one2 = 0x3F803F80u;   // two bf16 ones
     __nv_bfloat16* ext = reinterpret_cast<__nv_bfloat16*>(p.ws + (static_cast<size_t>(p.tiles) << 8));
     uint4* ea = reinterpret_cast<uint4*>(ext + ((2 * static_cast<size_t>(p.tiles)) << 7) * 16 +
@@ -372,9 +388,9 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     // No query sees these keys: their gradients are zero.
     if (threadIdx.x < 128) {
       const int j = w.kt * 128 + threadIdx.x;
-      if (j < w.sk.len) {
-        const int kpos = w.sk.base + j * w.sk.stride;
-        const size_t off = ((static_cast<size_t>(w.bat) * p.N + kpos) * p.G + w.g) * D;
+      const int kpos = w.sk.base + j * w.sk.stride;
+      const size_t off = ((static_cast<size_t>(w.bat) * p.N + kpos) * p.G + w.g) * D;
+      if (j < w.sk.len && in_bounds(off, D, kv_elems(p), p.status)) {
         uint4* a = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + off);
         uint4* b = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + off);
 #pragma unroll
@@ -621,6 +637,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       // dK = scale * sum dS^T Q, dV = sum A^T dO: this warp writes columns
       // [half * D/2, half * D/2 + D/2) of its key rows.
       const size_t off = ((static_cast<size_t>(w.bat) * p.N + (valid ? kpos : 0)) * p.G + w.g) * D;
+      const bool out_ok = valid && in_bounds(off, D, kv_elems(p), p.status);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float mul = which == 0 ? p.scale : 1.f;
@@ -631,7 +648,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
           const int col = half * (D / 2) + c * 32;
           uint32_t r[32];
           tmem_ld_x32(src + col, r);
-          if (valid) {
+          if (out_ok) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -743,10 +760,10 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
   if (T == 0) {
     if (threadIdx.x < 128) {
       const int i = w.qt * 128 + threadIdx.x;
-      if (i < w.sq.len) {
-        const int qpos = w.sq.base + i * w.sq.stride;
-        uint4* a = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) +
-                                            ((static_cast<size_t>(w.bat) * p.N + qpos) * p.H + w.h) * D);
+      const int qpos = w.sq.base + i * w.sq.stride;
+      const size_t off = ((static_cast<size_t>(w.bat) * p.N + qpos) * p.H + w.h) * D;
+      if (i < w.sq.len && in_bounds(off, D, q_elems(p), p.status)) {
+        uint4* a = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + off);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0u, 0u, 0u, 0u);
       }
@@ -889,8 +906,13 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
     const uint32_t tS = tmem + kColS + lane_off + half * 64;
     const uint32_t tDP = tmem + kColDP + lane_off + half * 64;
     const float* st_row = stats_tile(p, w.bat, w.h, w.sq.chunk, w.qt) + quarter * 32 + lane;
-    const float l2 = st_row[0];     // +inf past the chunk's end
-    const float drow = st_row[128];
+    const bool st_ok = in_bounds(static_cast<size_t>(st_row - p.ws), 129, stats_elems(p), p.status);
+    const float l2 = st_ok ? st_row[0] : INFINITY;     // +inf past the chunk's end
+    const float drow = st_ok ? st_row[128] : 0.f;
+    // this row of q, dout and dq lies in its tensor
+    const bool row_ok =
+        valid && in_bounds(((static_cast<size_t>(w.bat) * p.N + qpos) * p.H + w.h) * D, D,
+                           q_elems(p), p.status);
     const float2 cc = make_float2(p.scale_log2, p.scale_log2);
     const float2 ml = make_float2(-l2, -l2);
     const float2 dd = make_float2(drow, drow);
@@ -906,7 +928,7 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
         uint32_t r[32];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint4 x = valid ? src[c * 8 + j] : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 x = row_ok ? src[c * 8 + j] : make_uint4(0u, 0u, 0u, 0u);
           r[4 * j] = x.x;
           r[4 * j + 1] = x.y;
           r[4 * j + 2] = x.z;
@@ -984,7 +1006,7 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
         const int col = half * (D / 2) + c * 32;
         uint32_t r[32];
         tmem_ld_x32(tmem + kColDQ + lane_off + col, r);
-        if (valid) {
+        if (row_ok) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {

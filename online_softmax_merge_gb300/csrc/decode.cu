@@ -140,18 +140,21 @@ decode_mma_kernel(const __grid_constant__ RingParams p, const __grid_constant__ 
   uint32_t qa[KS][4];
   {
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    auto qrow = [&](int r) -> const uint32_t* {
+    auto qoff = [&](int r) -> size_t {
       const int rr = row0 + r, h = g * hpg + rr / n_q, t = rr % n_q;
-      return reinterpret_cast<const uint32_t*>(q + ((static_cast<size_t>(bat) * n_q + t) * p.H + h) * D);
+      return ((static_cast<size_t>(bat) * n_q + t) * p.H + h) * D;
     };
-    const uint32_t* ql = v_lo ? qrow(gid) : nullptr;
-    const uint32_t* qh = v_hi ? qrow(gid + 8) : nullptr;
+    const size_t q_n = static_cast<size_t>(p.B) * n_q * p.H * D;   // q is [B, n_q, H, d]
+    const bool q_lo = v_lo && in_bounds(qoff(gid), D, q_n, p.status);
+    const bool q_hi = v_hi && in_bounds(qoff(gid + 8), D, q_n, p.status);
+    const uint32_t* ql = q_lo ? reinterpret_cast<const uint32_t*>(q + qoff(gid)) : nullptr;
+    const uint32_t* qh = q_hi ? reinterpret_cast<const uint32_t*>(q + qoff(gid + 8)) : nullptr;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
-      qa[kk][0] = v_lo ? ql[8 * kk + tig] : 0u;
-      qa[kk][1] = v_hi ? qh[8 * kk + tig] : 0u;
-      qa[kk][2] = v_lo ? ql[8 * kk + 4 + tig] : 0u;
-      qa[kk][3] = v_hi ? qh[8 * kk + 4 + tig] : 0u;
+      qa[kk][0] = q_lo ? ql[8 * kk + tig] : 0u;
+      qa[kk][1] = q_hi ? qh[8 * kk + tig] : 0u;
+      qa[kk][2] = q_lo ? ql[8 * kk + 4 + tig] : 0u;
+      qa[kk][3] = q_hi ? qh[8 * kk + 4 + tig] : 0u;
     }
   }
 
@@ -330,11 +333,14 @@ decode_mma_kernel(const __grid_constant__ RingParams p, const __grid_constant__ 
       Y += f * sm_o[(w * kRows + r) * D + col];
     }
     const int rr = row0 + r, h = g * hpg + rr / n_q, t = rr % n_q;
+    // partials [parts, B, n_q, H, d] and [parts, B, H, n_q], parts = P * nseg * n_chunks
+    const size_t rows_n = static_cast<size_t>(p.P) * nseg * n_chunks * p.B * n_q * p.H;
     const size_t oo = (((static_cast<size_t>(part) * p.B + bat) * n_q + t) * p.H + h) * D + col;
-    o_parts[oo] = Z > 0.f ? Y / Z : 0.f;
+    if (in_bounds(oo, 1, rows_n * D, p.status)) o_parts[oo] = Z > 0.f ? Y / Z : 0.f;
     if (col == 0) {
       const size_t lo = ((static_cast<size_t>(part) * p.B + bat) * p.H + h) * n_q + t;
-      lse_parts[lo] = Z > 0.f ? (M + log2f(Z)) * kLn2 : -INFINITY;
+      if (in_bounds(lo, 1, rows_n, p.status))
+        lse_parts[lo] = Z > 0.f ? (M + log2f(Z)) * kLn2 : -INFINITY;
     }
   }
 }

@@ -8,6 +8,40 @@
 
 namespace ra {
 
+// Debug builds (compiled with -DRA_DEBUG): every raw global access (one that is not
+// a TMA copy, which the hardware bounds by its tensor map) first checks its element
+// range against the extent of its buffer. A failed check records RA_ERR_BOUNDS in
+// the status word and the access is skipped, so a wrong index shows up as a status
+// code rather than a memory fault. Release builds compile the checks away.
+#ifdef RA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+// Is [first, first + count) inside [0, extent)?
+__device__ __forceinline__ bool in_bounds(size_t first, size_t count, size_t extent,
+                                          int* status) {
+  if (!kDebugChecks) return true;
+  if (first <= extent && count <= extent - first) return true;
+  atomicCAS(status, 0, static_cast<int>(RA_ERR_BOUNDS));
+  return false;
+}
+
+// Element counts of the public tensors of a problem with fields B, N, H, G, D.
+template <typename Params>
+__host__ __device__ __forceinline__ size_t q_elems(const Params& p) {   // q, o, dout, dq, y
+  return static_cast<size_t>(p.B) * p.N * p.H * p.D;
+}
+template <typename Params>
+__host__ __device__ __forceinline__ size_t kv_elems(const Params& p) {  // k, v, dk, dv
+  return static_cast<size_t>(p.B) * p.N * p.G * p.D;
+}
+template <typename Params>
+__host__ __device__ __forceinline__ size_t row_elems(const Params& p) { // lse, m, z
+  return static_cast<size_t>(p.B) * p.H * p.N;
+}
+
 // Everything a ring kernel needs about one call. Sizes follow the public
 // conventions: q/o [B,N,H,d], k/v [B,N,G,d], lse/m/z [B,H,N], y [B,N,H,d].
 struct RingParams {
@@ -81,6 +115,7 @@ cudaError_t launch_tile_classes(const RingParams& p, int u, int b, int8_t* class
                                 cudaStream_t st);
 cudaError_t launch_mask(const RingParams& p, int u, int b, uint8_t* mask, cudaStream_t st);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t st);
+cudaError_t launch_selftest_bounds(int* status, cudaStream_t st);
 // Pass-Q decode, phase 1: per-(shard segment, key chunk) partials into the
 // workspace. tk, tv: [B,N,G,d] views with 32-row boxes.
 cudaError_t launch_decode_partials(const RingParams& p, const CUtensorMap& tk,

@@ -59,6 +59,13 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns, int* status) {
   if (threadIdx.x == 0 && !ok) atomicCAS(status, 0, static_cast<int>(RA_ERR_TIMEOUT));
 }
 
+// One thread checks the range [4, 5) against a 4-element extent (no access is made):
+// in a debug build the check fails and records RA_ERR_BOUNDS; in a release build the
+// check is compiled away and nothing is recorded.
+__global__ void selftest_bounds_kernel(int* status) {
+  if (threadIdx.x == 0) (void)in_bounds(4, 1, 4, status);
+}
+
 int blocks_for(long long n, int threads) {
   long long b = (n + threads - 1) / threads;
   if (b > 65535 * 16) b = 65535 * 16;
@@ -84,6 +91,11 @@ cudaError_t launch_tile_classes(const RingParams& p, int u, int b, int8_t* class
 cudaError_t launch_mask(const RingParams& p, int u, int b, uint8_t* mask, cudaStream_t st) {
   mask_kernel<<<blocks_for(static_cast<long long>(p.S) * p.S, 256), 256, 0, st>>>(
       p.layout, p.S, p.P, p.causal, u, b, mask);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_bounds(int* status, cudaStream_t st) {
+  selftest_bounds_kernel<<<1, 32, 0, st>>>(status);
   return cudaGetLastError();
 }
 

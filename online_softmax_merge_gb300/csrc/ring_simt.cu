@@ -45,7 +45,10 @@ ring_simt_kernel(const RingParams p, int s) {
   float m = -INFINITY, z = 0.f;
   const size_t md = valid ? (static_cast<size_t>(bat) * p.H + head) * p.N + qpos : 0;
   const size_t yo = valid ? ((static_cast<size_t>(bat) * p.N + qpos) * p.H + head) * D : 0;
-  if (valid && p.load_state) {
+  // this row's q, state and output lie in their tensors
+  const bool io_ok = valid && in_bounds(md, 1, row_elems(p), p.status) &&
+                     in_bounds(yo, D, q_elems(p), p.status);
+  if (io_ok && p.load_state) {
     m = p.m[md];
     z = p.z[md];
 #pragma unroll
@@ -55,7 +58,7 @@ ring_simt_kernel(const RingParams p, int s) {
     for (int e = 0; e < E; ++e) y[e] = 0.f;
   }
   for (int c = lane; c < D; c += 32)
-    qs[warp][c] = valid ? __bfloat162float(q[yo + c]) : 0.f;
+    qs[warp][c] = io_ok ? __bfloat162float(q[yo + c]) : 0.f;
 
   // keys that may be visible: a prefix of the shard except for zigzag (two runs)
   const int n_vis = !valid ? 0
@@ -76,9 +79,9 @@ ring_simt_kernel(const RingParams p, int s) {
       const int jj = idx / D, c = idx % D;
       const int j = j0 + jj;
       float kv = 0.f, vv = 0.f;
-      if (j < p.S) {
-        const int tk = pos_of(p.layout, p.S, p.P, b, j);
-        const size_t off = ((static_cast<size_t>(bat) * p.N + tk) * p.G + g) * D + c;
+      const int tk = j < p.S ? pos_of(p.layout, p.S, p.P, b, j) : 0;
+      const size_t off = ((static_cast<size_t>(bat) * p.N + tk) * p.G + g) * D + c;
+      if (j < p.S && in_bounds(off, 1, kv_elems(p), p.status)) {
         kv = __bfloat162float(k[off]);
         vv = __bfloat162float(v[off]);
       }
@@ -113,7 +116,7 @@ ring_simt_kernel(const RingParams p, int s) {
     }
     m = m_new;
   }
-  if (valid) {
+  if (io_ok) {
 #pragma unroll
     for (int e = 0; e < E; ++e) p.y[yo + lane + 32 * e] = y[e];
     if (lane == 0) {

@@ -211,13 +211,14 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     if (p.step_mode && !p.load_state && threadIdx.x < 256) {
       const int i = threadIdx.x >> 7;
       const int row = w.row0[i] + (threadIdx.x & 127);
-      if (row < sq.len) {
-        const int tok = sq.base + row * sq.stride;
-        const size_t md = (static_cast<size_t>(w.bat) * p.H + w.head[i]) * p.N + tok;
+      const int tok = sq.base + row * sq.stride;
+      const size_t md = (static_cast<size_t>(w.bat) * p.H + w.head[i]) * p.N + tok;
+      const size_t y0 = ((static_cast<size_t>(w.bat) * p.N + tok) * p.H + w.head[i]) * D;
+      if (row < sq.len && in_bounds(md, 1, row_elems(p), p.status) &&
+          in_bounds(y0, D, q_elems(p), p.status)) {
         p.m[md] = -INFINITY;
         p.z[md] = 0.f;
-        float4* yr = reinterpret_cast<float4*>(
-            p.y + ((static_cast<size_t>(w.bat) * p.N + tok) * p.H + w.head[i]) * D);
+        float4* yr = reinterpret_cast<float4*>(p.y + y0);
 #pragma unroll
         for (int c = 0; c < D / 4; ++c) yr[c] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -413,12 +414,15 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     const uint32_t tO = tmem + L::kOcol + i * D + lane_off;
     const size_t md = valid ? (static_cast<size_t>(w.bat) * p.H + head) * p.N + qpos : 0;
     const size_t yo = valid ? ((static_cast<size_t>(w.bat) * p.N + qpos) * p.H + head) * D : 0;
+    // this row's global reads and writes (O, LSE, or the state m, z, y) stay in bounds
+    const bool io_ok = valid && in_bounds(md, 1, row_elems(p), p.status) &&
+                       in_bounds(yo, D, q_elems(p), p.status);
     const float c2 = p.scale_log2;
     float m_run = -INFINITY;   // running max of the scaled scores, log2 units
     float z_run = 0.f;         // running denominator
 
     if (p.step_mode && p.load_state) {
-      if (valid) {
+      if (io_ok) {
         const float mm = p.m[md];
         m_run = (mm == -INFINITY) ? -INFINITY : mm * kLog2e;
         z_run = p.z[md];
@@ -426,7 +430,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t buf[32];
-        if (valid) {
+        if (io_ok) {
           const float4* src = reinterpret_cast<const float4*>(p.y + yo + c * 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -568,7 +572,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld_x32(tO + c * 32, r);
-          if (valid) {
+          if (io_ok) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + yo + c * 32);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -581,13 +585,13 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
             }
           }
         }
-        if (valid) p.lse[md] = z_run > 0.f ? (m_run + log2f(z_run)) * kLn2 : -INFINITY;
+        if (io_ok) p.lse[md] = z_run > 0.f ? (m_run + log2f(z_run)) * kLn2 : -INFINITY;
       } else {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld_x32(tO + c * 32, r);
-          if (valid) {
+          if (io_ok) {
             float4* dst = reinterpret_cast<float4*>(p.y + yo + c * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -595,7 +599,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
           }
         }
-        if (valid) {
+        if (io_ok) {
           p.m[md] = (m_run == -INFINITY) ? -INFINITY : m_run * kLn2;
           p.z[md] = z_run;
         }

@@ -37,6 +37,18 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.ring_attn_version() == 100
 
 
+def test_debug_build_exports_the_same_symbols_and_reports_its_checks(lib):
+    """libringattn_debug.so (the kernels with index checks) has the same ABI; only
+    ring_attn_debug_checks tells the two apart."""
+    dbg = ctypes.CDLL(B.build(debug=True))
+    for name in _declared():
+        assert hasattr(dbg, name), name
+    dbg.ring_attn_debug_checks.restype = ctypes.c_int32
+    assert dbg.ring_attn_debug_checks() == 1
+    if os.environ.get("RA_DEBUG") != "1":
+        assert lib.ring_attn_debug_checks() == 0
+
+
 def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert lib.ra_status_str(code).decode() == name
