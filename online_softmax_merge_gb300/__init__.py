@@ -47,6 +47,13 @@ def _need(t: torch.Tensor, name: str, dtype, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _same_device(ref: torch.Tensor, **tensors):
+    """Every tensor passed by name lives on ref's GPU (the kernels are launched there)."""
+    for name, t in tensors.items():
+        if t.device != ref.device:
+            raise ValueError(f"{name} is on {t.device}, the call runs on {ref.device}")
+
+
 def problem(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int, P: int,
             causal: bool, layout: str = "contiguous", scale: float = 0.0) -> _lib.RaProblem:
     """The ra_problem struct (scale 0 means 1/sqrt(head_dim))."""
@@ -81,6 +88,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str =
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.bfloat16, (B, N, H, d))
     _need(lse, "lse", torch.float32, (B, H, N))
+    _same_device(q, out=out, lse=lse)
     with torch.cuda.device(q.device):
         check("ring_attn_fwd", lib.ring_attn_fwd(ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v),
                                                  _ptr(out), _ptr(lse), _stream(q.device)))
@@ -92,8 +100,8 @@ def _need_host(t: torch.Tensor, name: str, dtype, shape):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if t.is_cuda:
-        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor, got {t.device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if tuple(t.shape) != tuple(shape):
@@ -135,6 +143,8 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    if workspace.device != dev:
+        raise ValueError(f"workspace is on {workspace.device}, the call runs on {dev}")
     pin = q.is_pinned()
     if out is None:
         out = torch.empty((B, N, H, d), dtype=torch.bfloat16, pin_memory=pin)
@@ -187,6 +197,7 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     _need(dq, "dq", torch.bfloat16, (B, N, H, d))
     _need(dk, "dk", torch.bfloat16, (B, N, G, d))
     _need(dv, "dv", torch.bfloat16, (B, N, G, d))
+    _same_device(q, o=o, lse=lse, dout=dout, workspace=workspace, dq=dq, dk=dk, dv=dv)
     with torch.cuda.device(q.device):
         check("ring_attn_bwd", lib.ring_attn_bwd(
             ctypes.byref(pr), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
@@ -228,6 +239,7 @@ def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, q_pos0: in
         lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
     _need(out, "out", torch.bfloat16, (B, n_q, H, d))
     _need(lse, "lse", torch.float32, (B, H, n_q))
+    _same_device(q, k=k, v=v, workspace=workspace, out=out, lse=lse)
     with torch.cuda.device(q.device):
         check("ring_attn_decode", lib.ring_attn_decode(
             ctypes.byref(pr), int(n_q), int(q_pos0), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
@@ -252,6 +264,7 @@ def _step(fn_name, q, k, v, P, s, state, first, layout, causal, scale):
     _need(m, "m", torch.float32, (B, H, N))
     _need(z, "z", torch.float32, (B, H, N))
     _need(y, "y", torch.float32, (B, N, H, d))
+    _same_device(q, m=m, z=z, y=y)
     with torch.cuda.device(q.device):
         check(fn_name, getattr(lib, fn_name)(ctypes.byref(pr), int(s), int(bool(first)), _ptr(q),
                                              _ptr(k), _ptr(v), _ptr(m), _ptr(z), _ptr(y),
@@ -286,6 +299,7 @@ def finalize(state, P: int = 1, layout: str = "contiguous", causal: bool = True,
         lse = torch.empty((B, H, N), dtype=torch.float32, device=y.device)
     _need(out, "out", torch.bfloat16, (B, N, H, d))
     _need(lse, "lse", torch.float32, (B, H, N))
+    _same_device(y, m=m, z=z, out=out, lse=lse)
     pr = problem(B, N, H, H, d, P, causal, layout)
     with torch.cuda.device(y.device):
         check("ring_attn_finalize", lib.ring_attn_finalize(ctypes.byref(pr), _ptr(m), _ptr(z),
@@ -309,6 +323,7 @@ def merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: Optional[torch.Te
         lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device)
     _need(out, "out", torch.bfloat16, (B, N, H, d))
     _need(lse, "lse", torch.float32, (B, H, N))
+    _same_device(o_parts, lse_parts=lse_parts, out=out, lse=lse)
     with torch.cuda.device(o_parts.device):
         check("ring_attn_merge", lib.ring_attn_merge(n, B, N, H, d, _ptr(o_parts), _ptr(lse_parts),
                                                      _ptr(out), _ptr(lse),
