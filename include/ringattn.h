@@ -51,7 +51,10 @@
  *  the eager call would on the buffers' contents at replay time.
  *
  *  Errors: argument errors are returned synchronously before any launch and
- *  nothing is written. RA_ERR_CUDA means a CUDA call (launch or tensor-map
+ *  nothing is written. Every device pointer is checked to be memory the current
+ *  device's kernels may touch (its device memory — cudaMalloc, pools, virtual-memory
+ *  mappings — or managed memory); host memory and other devices' memory give
+ *  RA_ERR_INVALID_ARG instead of a kernel that would fault. RA_ERR_CUDA means a CUDA call (launch or tensor-map
  *  encode) failed. A device-side wait that exceeds its time limit makes the
  *  kernel stop early and record RA_ERR_TIMEOUT in the status word, read with
  *  ring_attn_last_error() after synchronising the stream. Nothing throws.
@@ -68,7 +71,8 @@ extern "C" {
 
 typedef enum {
   RA_OK = 0,
-  RA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, N % P != 0, H % G != 0, misaligned */
+  RA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, N % P != 0, H % G != 0, misaligned,
+                               or a device pointer that is not memory of the current device */
   RA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, no sm_103a device, or a size past a
                                launch limit (e.g. batch x heads x P x query tiles >= 2^31) */
   RA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */

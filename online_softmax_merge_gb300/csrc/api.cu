@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 #include <new>
 
@@ -23,6 +24,7 @@ constexpr int kMaxDevices = 64;
 struct DevInfo {
   bool init = false;
   bool sm103 = false;
+  int ordinal = -1;
   int* status = nullptr;
 };
 std::mutex g_mu;
@@ -41,6 +43,7 @@ ra_status current_device(DevInfo** out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return RA_ERR_CUDA;
     d.sm103 = (major == 10 && minor == 3);
+    d.ordinal = dev;
     if (d.sm103) {
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return RA_ERR_CUDA;
@@ -53,6 +56,24 @@ ra_status current_device(DevInfo** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Memory the kernels launched on the current device may touch: device memory of that
+// device (cudaMalloc, stream-ordered pools, virtual-memory mappings) or managed memory.
+// Host memory (pageable or pinned) and other devices' memory are refused before
+// anything is launched, since a kernel reading them could fault the GPU.
+ra_status resident(const DevInfo* d, std::initializer_list<const void*> ptrs) {
+  for (const void* ptr : ptrs) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+      (void)cudaGetLastError();   // the failed query leaves a (non-sticky) error behind
+      return RA_ERR_INVALID_ARG;
+    }
+    const bool ok = a.type == cudaMemoryTypeManaged ||
+                    (a.type == cudaMemoryTypeDevice && a.device == d->ordinal);
+    if (!ok) return RA_ERR_INVALID_ARG;
+  }
+  return RA_OK;
+}
 
 ra_status check_layout_sizes(int32_t layout, int32_t seqlen, int32_t P) {
   if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED && layout != RA_LAYOUT_ZIGZAG)
@@ -279,6 +300,7 @@ ra_status ring_attn_fwd(const ra_problem* pr, const void* q, const void* k, cons
     return RA_ERR_INVALID_ARG;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {q, k, v, o, lse})) != RA_OK) return st;
   RingParams p;
   fill_params(pr, &p);
   p.s_begin = 0;
@@ -307,6 +329,7 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   if (workspace_bytes < fwd_host_workspace(pr)) return RA_ERR_INVALID_ARG;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {workspace})) != RA_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
   const HostSlot hs = host_slot(pr);
@@ -403,6 +426,7 @@ ra_status ring_attn_step(const ra_problem* pr, int32_t s, int32_t first, const v
   if (st != RA_OK) return st;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {q, k, v, m, z, y})) != RA_OK) return st;
   RingParams p;
   fill_params(pr, &p);
   p.s_begin = s;
@@ -428,6 +452,7 @@ ra_status ring_attn_step_simt(const ra_problem* pr, int32_t s, int32_t first, co
     return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {q, k, v, m, z, y})) != RA_OK) return st;
   RingParams p;
   fill_params(pr, &p);
   p.s_begin = s;
@@ -454,6 +479,7 @@ ra_status ring_attn_finalize(const ra_problem* pr, const float* m, const float* 
   if (static_cast<long long>(pr->batch) > 65535 || pr->heads > 65535) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {m, z, y, o, lse})) != RA_OK) return st;
   RingParams p;
   fill_params(pr, &p);
   p.m = const_cast<float*>(m);
@@ -478,6 +504,7 @@ ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_
   DevInfo* d = nullptr;
   ra_status st = current_device(&d);
   if (st != RA_OK) return st;
+  if ((st = resident(d, {o_parts, lse_parts, o, lse})) != RA_OK) return st;
   return launch_result(launch_merge(n_parts, batch, seqlen, heads, head_dim, o_parts, lse_parts,
                                     o, lse, static_cast<cudaStream_t>(stream)));
 }
@@ -502,6 +529,7 @@ ra_status ring_attn_shard_map_device(int32_t layout, int32_t seqlen, int32_t P, 
   DevInfo* d = nullptr;
   ra_status st = current_device(&d);
   if (st != RA_OK) return st;
+  if ((st = resident(d, {owner, local, token_of})) != RA_OK) return st;
   return launch_result(
       launch_shard_map(layout, seqlen, P, owner, local, token_of, static_cast<cudaStream_t>(stream)));
 }
@@ -513,6 +541,7 @@ ra_status ring_attn_tile_classes(const ra_problem* pr, int32_t u, int32_t b, int
   if (u < 0 || u >= pr->P || b < 0 || b >= pr->P || classes == nullptr) return RA_ERR_INVALID_ARG;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {classes})) != RA_OK) return st;
   RingParams p;
   fill_params(pr, &p);
   return launch_result(launch_tile_classes(p, u, b, classes, static_cast<cudaStream_t>(stream)));
@@ -525,6 +554,7 @@ ra_status ring_attn_mask(const ra_problem* pr, int32_t u, int32_t b, uint8_t* ma
   if (u < 0 || u >= pr->P || b < 0 || b >= pr->P || mask == nullptr) return RA_ERR_INVALID_ARG;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {mask})) != RA_OK) return st;
   RingParams p;
   fill_params(pr, &p);
   return launch_result(launch_mask(p, u, b, mask, static_cast<cudaStream_t>(stream)));
@@ -553,6 +583,7 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
   if (bwd_tiles(pr) * 2 * 128 + 128 >= (static_cast<int64_t>(1) << 31)) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {q, k, v, o, lse, dout, dq, dk, dv, workspace})) != RA_OK) return st;
   RingParams f;
   fill_params(pr, &f);
   BwdParams p;
@@ -619,6 +650,7 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
     return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
+  if ((st = resident(d, {q, k, v, o, lse, workspace})) != RA_OK) return st;
   RingParams p;
   fill_params(pr, &p);
   p.q = q;
