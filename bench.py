@@ -607,7 +607,7 @@ def main():
     ap.add_argument("--layout", default=None, choices=[None, "contiguous", "striped", "zigzag"])
     ap.add_argument("--P", type=int, default=None, help="override the preset's shard count")
     ap.add_argument("--seed", type=int, default=None, help="override the preset's input seed")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--one-core-seconds", type=float, default=6.0)

@@ -125,30 +125,37 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
  * from, o and lse written to, host memory (page-locked memory lets the copies
  * overlap the kernels; pageable memory also works, with the copies serialised).
  * The work goes through the GPU in pieces — one sequence's query heads of one
- * kv group with that kv head — in two device slots of the workspace: while piece
- * i is computed on `stream`, the inputs of piece i + 1 travel in and the outputs
- * of piece i - 1 travel out on `copy_stream` (strided copies gather a group's
- * heads), so only the first piece's inputs and the last one's outputs are not
- * hidden behind compute. Each piece is exactly a ring_attn_fwd call on its
- * heads (the results equal ring_attn_fwd bit for bit). Work enqueued on `stream`
- * before the call happens before any of its copies, and `stream` completes only
- * once the outputs are in host memory, so synchronising `stream` is enough; that
- * holds after an error returned midway too (`stream` still waits for every copy
- * already queued) before the workspace or host buffers are reused. The call
- * returns after enqueuing; it creates and releases its ordering events itself. There is no counterpart in
- * the pages: this is an interface choice of this library (host-resident inputs,
- * e.g. in the CPU memory of a Grace host).
+ * kv group with that kv head — in as many device slots as the workspace holds
+ * (at least two): while piece i is computed on `stream`, the inputs of the next
+ * pieces travel in on `copy_stream` as soon as their slot is free (up to
+ * slots - 1 pieces ahead), and the outputs of finished pieces travel out on a
+ * stream the call creates and releases itself (strided copies gather a group's
+ * heads). Only the first piece's inputs and the last one's outputs are not hidden
+ * behind compute, and the slack of the extra slots absorbs a copy that stalls
+ * (host-link copies were seen to stall for tens of milliseconds while the GPU
+ * changed clocks under its power cap). Each piece is exactly a ring_attn_fwd
+ * call on its heads (the results equal ring_attn_fwd bit for bit). Work enqueued
+ * on `stream` before the call happens before any of its copies, and `stream`
+ * completes only once the outputs are in host memory, so synchronising `stream`
+ * is enough; that holds after an error returned midway too (`stream` still waits
+ * for every copy already queued) before the workspace or host buffers are reused.
+ * The call returns after enqueuing; it creates and releases its ordering events
+ * and its output stream itself. There is no counterpart in the pages: this is an
+ * interface choice of this library (host-resident inputs, e.g. in the CPU memory
+ * of a Grace host).
  * q, k, v, o, lse: host pointers in the shapes of ring_attn_fwd. workspace:
- * device memory of at least ring_attn_fwd_host_workspace_bytes(p) bytes,
- * 16-byte aligned, overwritten. copy_stream may equal stream (no overlap). */
+ * device memory of this device, 16-byte aligned, overwritten, of at least two
+ * slots (ring_attn_fwd_host_workspace_bytes gives room for eight). copy_stream
+ * may equal stream (the input copies then do not overlap the kernels). */
 ra_status ring_attn_fwd_host(const ra_problem* p, const void* q, const void* k, const void* v,
                              void* o, float* lse, void* workspace, size_t workspace_bytes,
                              void* stream, void* copy_stream);
 
-/* Bytes of device workspace ring_attn_fwd_host needs: two pieces' q, k, v, o,
- * lse (one piece if batch * kv_heads is 1), each rounded up to 256 bytes. A piece
- * holds seqlen tokens of heads/kv_heads query heads and one kv head. Pure host
- * code. */
+/* Recommended bytes of device workspace for ring_attn_fwd_host: eight slots (or
+ * one per piece if batch * kv_heads is smaller), a slot being one piece's q, k, v,
+ * o, lse, each rounded up to 256 bytes. A piece holds seqlen tokens of
+ * heads/kv_heads query heads and one kv head. Any workspace of at least two slots
+ * is accepted; the call uses as many slots as it holds. Pure host code. */
 size_t ring_attn_fwd_host_workspace_bytes(const ra_problem* p);
 
 /* One ring step for all virtual devices at once: device u folds shard

@@ -282,9 +282,20 @@ HostSlot host_slot(const ra_problem* pr) {
   s.total = s.q + 2 * s.kv + s.o + s.lse;
   return s;
 }
+// Device slots of ring_attn_fwd_host: at least 2 (or one per piece if fewer) are
+// required; the recommended workspace holds kHostSlots, so the input copies can run
+// up to kHostSlots - 1 pieces ahead of the kernels and absorb a stalled copy.
+constexpr int64_t kHostSlots = 8;
+int64_t host_pieces(const ra_problem* pr) {
+  return static_cast<int64_t>(pr->batch) * pr->kv_heads;
+}
+size_t fwd_host_min_workspace(const ra_problem* pr) {
+  const int64_t n = host_pieces(pr);
+  return host_slot(pr).total * static_cast<size_t>(n < 2 ? n : 2);
+}
 size_t fwd_host_workspace(const ra_problem* pr) {
-  const int64_t pieces = static_cast<int64_t>(pr->batch) * pr->kv_heads;
-  return host_slot(pr).total * static_cast<size_t>(pieces < 2 ? pieces : 2);
+  const int64_t n = host_pieces(pr);
+  return host_slot(pr).total * static_cast<size_t>(n < kHostSlots ? n : kHostSlots);
 }
 
 }  // namespace
@@ -326,15 +337,19 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   if (st != RA_OK) return st;
   if (!q || !k || !v || !o || !lse || !workspace || !aligned16(workspace))
     return RA_ERR_INVALID_ARG;
-  if (workspace_bytes < fwd_host_workspace(pr)) return RA_ERR_INVALID_ARG;
+  if (workspace_bytes < fwd_host_min_workspace(pr)) return RA_ERR_INVALID_ARG;
+  if (host_pieces(pr) > (1 << 24)) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
   if ((st = resident(d, {workspace})) != RA_OK) return st;
-  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const cudaStream_t xs = static_cast<cudaStream_t>(copy_stream);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);        // kernels
+  const cudaStream_t is = static_cast<cudaStream_t>(copy_stream);   // inputs in
   const HostSlot hs = host_slot(pr);
   const int B = pr->batch, G = pr->kv_heads, H = pr->heads, N = pr->seqlen, D = pr->head_dim;
   const int hpg = H / G;
+  const int n = static_cast<int>(host_pieces(pr));
+  const int64_t fit = static_cast<int64_t>(workspace_bytes / hs.total);
+  const int S = static_cast<int>(fit < n ? fit : n);                // device slots in use
   // A piece (b, g) is the ring forward of sequence b restricted to kv group g:
   // its query heads [g hpg, (g+1) hpg) against kv head g, a problem of its own.
   ra_problem one = *pr;
@@ -351,40 +366,47 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   const size_t w_q = static_cast<size_t>(hpg) * D * 2;      // a piece's bytes per token
   const size_t w_kv = static_cast<size_t>(D) * 2;
   const size_t lse_piece = static_cast<size_t>(hpg) * N * sizeof(float);
-  if (static_cast<int64_t>(B) * G > (1 << 24)) return RA_ERR_UNSUPPORTED;
-  const int n_pieces = B * G;
-  // events: start (stream -> copy_stream), end, inputs in[i], kernel done k[i]
-  const int n_ev = 2 + 2 * n_pieces;
+  // Outputs leave on a stream of this call's own, so a stalled output copy never
+  // holds up the input copies (and the reverse).
+  cudaStream_t os = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&os, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return RA_ERR_CUDA;
+  // events: start, inputs-done joined back, end; per piece: inputs in, kernel done, outputs out
+  const int n_ev = 3 + 3 * n;
   cudaEvent_t* ev = new (std::nothrow) cudaEvent_t[n_ev];
-  if (ev == nullptr) return RA_ERR_CUDA;
+  if (ev == nullptr) {
+    cudaStreamDestroy(os);
+    return RA_ERR_CUDA;
+  }
   int made = 0;
-  cudaError_t e = cudaSuccess;
   for (; made < n_ev && e == cudaSuccess; ++made)
     e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
   if (e != cudaSuccess) --made;
-  cudaEvent_t ev_start = ev[0], ev_end = ev[1];
-  auto ev_in = [&](int i) { return ev[2 + i]; };
-  auto ev_k = [&](int i) { return ev[2 + n_pieces + i]; };
-  auto slot = [&](int i) { return static_cast<uint8_t*>(workspace) + (i % 2) * hs.total; };
+  const cudaEvent_t ev_start = ev[0], ev_in_end = ev[1], ev_end = ev[2];
+  auto ev_in = [&](int i) { return ev[3 + i]; };
+  auto ev_k = [&](int i) { return ev[3 + n + i]; };
+  auto ev_out = [&](int i) { return ev[3 + 2 * n + i]; };
+  auto slot = [&](int i) { return static_cast<uint8_t*>(workspace) + (i % S) * hs.total; };
   auto h2d = [&](int i) -> cudaError_t {
     const int b = i / G, g = i % G;
     uint8_t* s0 = slot(i);
     const uint8_t* qs = static_cast<const uint8_t*>(q) + static_cast<size_t>(b) * N * row_q + g * w_q;
     const uint8_t* ks = static_cast<const uint8_t*>(k) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
     const uint8_t* vs = static_cast<const uint8_t*>(v) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
-    cudaError_t r = cudaMemcpy2DAsync(s0, w_q, qs, row_q, w_q, N, cudaMemcpyHostToDevice, xs);
+    cudaError_t r = cudaMemcpy2DAsync(s0, w_q, qs, row_q, w_q, N, cudaMemcpyHostToDevice, is);
     if (r == cudaSuccess)
-      r = cudaMemcpy2DAsync(s0 + hs.q, w_kv, ks, row_kv, w_kv, N, cudaMemcpyHostToDevice, xs);
+      r = cudaMemcpy2DAsync(s0 + hs.q, w_kv, ks, row_kv, w_kv, N, cudaMemcpyHostToDevice, is);
     if (r == cudaSuccess)
       r = cudaMemcpy2DAsync(s0 + hs.q + hs.kv, w_kv, vs, row_kv, w_kv, N, cudaMemcpyHostToDevice,
-                            xs);
-    if (r == cudaSuccess) r = cudaEventRecord(ev_in(i), xs);
+                            is);
+    if (r == cudaSuccess) r = cudaEventRecord(ev_in(i), is);
     return r;
   };
   if (e == cudaSuccess) e = cudaEventRecord(ev_start, cs);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, ev_start, 0);
-  for (int i = 0; i < n_pieces && i < 2 && e == cudaSuccess; ++i) e = h2d(i);
-  for (int i = 0; i < n_pieces && e == cudaSuccess; ++i) {
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(is, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(os, ev_start, 0);
+  for (int i = 0; i < S && e == cudaSuccess; ++i) e = h2d(i);        // fill every slot
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
     const int b = i / G, g = i % G;
     uint8_t* s0 = slot(i);
     e = cudaStreamWaitEvent(cs, ev_in(i), 0);
@@ -396,25 +418,32 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
     p.lse = reinterpret_cast<float*>(s0 + hs.q + 2 * hs.kv + hs.o);
     if ((st = run_tc(p, cs)) != RA_OK) break;
     e = cudaEventRecord(ev_k(i), cs);
-    // outputs of piece i out, then (its slot free) the inputs of piece i + 2 in
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(xs, ev_k(i), 0);
+    // outputs of piece i out once its kernel is done
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(os, ev_k(i), 0);
     if (e == cudaSuccess)
       e = cudaMemcpy2DAsync(static_cast<uint8_t*>(o) + static_cast<size_t>(b) * N * row_q + g * w_q, row_q, p.o, w_q, w_q,
-                            N, cudaMemcpyDeviceToHost, xs);
+                            N, cudaMemcpyDeviceToHost, os);
     if (e == cudaSuccess)   // lse [B, H, N]: the group's heads are consecutive rows
       e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + (static_cast<size_t>(b) * G + g) * lse_piece,
-                          p.lse, lse_piece, cudaMemcpyDeviceToHost, xs);
-    if (e == cudaSuccess && i + 2 < n_pieces) e = h2d(i + 2);
+                          p.lse, lse_piece, cudaMemcpyDeviceToHost, os);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out(i), os);
+    // the slot is free once its outputs are out (its inputs were consumed before):
+    // the inputs of piece i + S come in there
+    if (e == cudaSuccess && i + S < n) e = cudaStreamWaitEvent(is, ev_out(i), 0);
+    if (e == cudaSuccess && i + S < n) e = h2d(i + S);
   }
-  // Join the copy stream back into `stream`, also after an error: copies already queued
-  // may still write the workspace, and the caller orders its reuse on `stream`.
+  // Join both copy streams back into `stream`, also after an error: copies already
+  // queued may still write the workspace, and the caller orders its reuse on `stream`.
   if (made == n_ev) {
-    const cudaError_t j = cudaEventRecord(ev_end, xs);
-    const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(cs, ev_end, 0) : j;
-    if (e == cudaSuccess) e = w;
+    cudaError_t j = cudaEventRecord(ev_in_end, is);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(cs, ev_in_end, 0);
+    if (j == cudaSuccess) j = cudaEventRecord(ev_end, os);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(cs, ev_end, 0);
+    if (e == cudaSuccess) e = j;
   }
   for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);   // released once they complete
   delete[] ev;
+  cudaStreamDestroy(os);                                      // likewise
   if (st != RA_OK) return st;
   return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }

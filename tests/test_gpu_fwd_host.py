@@ -1,7 +1,8 @@
 """ring_attn_fwd_host: the ring forward for inputs in host memory, pipelined one
-(sequence, kv group) piece at a time through two device slots. Each piece is a
+(sequence, kv group) piece at a time through the workspace's device slots (inputs in
+on the copy stream, outputs out on a stream of the call's own). Each piece is a
 ring_attn_fwd call on its heads, so the results must equal the device path bit for
-bit."""
+bit, whatever the number of slots."""
 import pytest
 import torch
 
@@ -57,6 +58,25 @@ def test_host_forward_with_explicit_scale():
     o_h, l_h = ra.fwd_host(q, k, v, w.P, w.layout, w.causal, scale=0.3, device=DEV)
     torch.cuda.synchronize()
     o_d, l_d = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal, 0.3)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())
+
+
+@pytest.mark.parametrize("slots", [2, 3, 5])
+def test_host_forward_with_fewer_slots_than_pieces(slots):
+    """Eight pieces through 2, 3 or 5 slots: every slot is refilled while others are
+    in use, at every stride."""
+    w = Workload("hostslots", 4, 4 * 150, 4, 2, 128, 4, "contiguous", True, 430)
+    q, k, v = (t.pin_memory() for t in make_qkv(w))
+    full = ra.fwd_host_workspace_bytes(w.batch, w.seqlen, w.heads, w.kv_heads, w.head_dim,
+                                       w.P, w.layout, w.causal)
+    slot = full // 8                                      # 8 pieces: the default holds 8 slots
+    ws = torch.empty(slots * slot, dtype=torch.uint8, device=DEV)
+    o_h, l_h = ra.fwd_host(q, k, v, w.P, w.layout, w.causal, workspace=ws, device=DEV)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    o_d, l_d = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal)
     torch.cuda.synchronize()
     assert torch.equal(o_h, o_d.cpu())
     assert torch.equal(l_h, l_d.cpu())
