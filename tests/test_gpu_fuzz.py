@@ -37,9 +37,16 @@ def draw(i: int) -> Workload:
     return Workload(f"fuzz{i}", B, P * S, G * hpg, G, d, P, layout, causal, 6000 + i)
 
 
-CASES = [draw(i) for i in range(N_CASES)]
-IDS = [f"{i}-{w.layout}-{'c' if w.causal else 'n'}-d{w.head_dim}-H{w.heads}G{w.kv_heads}"
-       f"-P{w.P}-S{w.shard_len}-B{w.batch}" for i, w in enumerate(CASES)]
+CASES = [draw(i) for i in range(N_CASES)] + [
+    # wide head groupings: 64 query heads on one kv head (32 head pairs per CTA group,
+    # 64 decode rows per kv head), 48 heads MHA, 64 over 4
+    Workload("wide-mqa", 1, 2 * 300, 64, 1, 64, 2, "striped", True, 6100),
+    Workload("wide-mha", 1, 3 * 160, 48, 48, 128, 3, "contiguous", True, 6101),
+    Workload("wide-gqa16", 2, 4 * 96, 64, 4, 128, 4, "zigzag", True, 6102),
+]
+IDS = [f"{w.name}-{w.layout}-{'c' if w.causal else 'n'}-d{w.head_dim}-H{w.heads}G{w.kv_heads}"
+       f"-P{w.P}-S{w.shard_len}-B{w.batch}" for w in CASES]
+WIDE = CASES[N_CASES:]
 
 
 def test_draws_cover_the_edge_shapes():
@@ -76,7 +83,7 @@ def test_fuzz_forward_and_backward(w):
         assert em <= TOL_GRAD_MAX and ef <= TOL_GRAD_FRO, (name, em, ef)
 
 
-@pytest.mark.parametrize("w", CASES[::3], ids=IDS[::3])
+@pytest.mark.parametrize("w", CASES[:N_CASES:3] + WIDE, ids=IDS[:N_CASES:3] + IDS[N_CASES:])
 def test_fuzz_decode(w):
     """The last two tokens (or one, for one-token sequences) as decode queries."""
     _, k, v = make_qkv(w)
