@@ -40,7 +40,8 @@
  *  ring_attn_decode_noalloc. `stream` is a cudaStream_t (NULL = legacy default
  *  stream); every call that takes one is asynchronous on it. Calls on one
  *  stream are ordered; the library holds no per-call host state beyond the
- *  ordering events ring_attn_fwd_host creates and releases itself, so
+ *  ordering events and the output-copy stream that ring_attn_fwd_host creates
+ *  and releases itself, so
  *  concurrent calls on different streams are safe when their output buffers
  *  (and workspaces) do not overlap.
  *
