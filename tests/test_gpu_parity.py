@@ -12,6 +12,7 @@ import torch
 
 from gpu_helpers import TOL_LSE, TOL_O, compare_full, host32
 from online_softmax_merge_gb300.inputs import Workload, make_qkv
+from oracle import attention as OA
 
 pytestmark = pytest.mark.gpu
 
@@ -147,3 +148,31 @@ def test_repeated_calls_are_deterministic():
     o2, l2 = ra.fwd(q, k, v, w.P, w.layout, True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("factor", [4, 16, 64])
+def test_large_logits_stay_within_the_arithmetic_bounds(factor):
+    """Q and K scaled by `factor` (score spread ~ factor^2), past the configurations'
+    inputs. The errors follow the arithmetic, not the N(0, 1) bars:
+      * LSE: each score is an fp32 sum of d products, so its rounding error is of the
+        order 2^-24 sum_k |q_k k_k| scale; the bound allows 2^-21 of it (8x).
+      * O: P is rounded to bf16 for the tensor core (relative 2^-9, at most 2^-9 max|V|
+        in O) and O itself to bf16 (half an ulp, at most 2^-8 |O|)."""
+    w = Workload("big", 1, 4 * 300, 4, 2, 128, 4, "contiguous", True, 950)
+    q, k, v = make_qkv(w)
+    q = (q.float() * factor).to(torch.bfloat16)
+    k = (k.float() * factor).to(torch.bfloat16)
+    o, lse = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    hq, hk, hv = (t.double().numpy() for t in (q, k, v))
+    O, L = OA.dense_attention(hq, hk, hv, True)
+    scale = 1.0 / np.sqrt(w.head_dim)
+    dot_mag = 0.0
+    for h in range(w.heads):
+        g = h * w.kv_heads // w.heads
+        dot_mag = max(dot_mag, float((np.abs(hq[0, :, h]) @ np.abs(hk[0, :, g]).T).max()) * scale)
+    el = float(np.abs(host32(lse) - L).max())
+    eo = float(np.abs(host32(o) - O).max())
+    assert el <= 2.0 ** -21 * dot_mag + 1e-6, (el, dot_mag)
+    assert eo <= 2.0 ** -9 * float(np.abs(hv).max()) + 2.0 ** -8 * float(np.abs(O).max()) + 1e-4, eo
