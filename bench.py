@@ -264,6 +264,33 @@ def oracle_rate(q, k, v, w, seconds: float, workers: int, windows: int = 1, seed
              sum(r["rows"][i] for r in results)) for i in range(windows)]
 
 
+def oracle_spot_check(q, k, v, o, lse, w, n_rows: int = 16, seed: int = 7):
+    """Max |O - O_oracle| and |LSE - LSE_oracle| of the timed forward's own output on
+    n_rows seeded query rows of the last sequence (the largest memory offsets), for
+    query heads 0, H/3, 2H/3, H-1, against the fp64 oracle."""
+    from oracle.attention import attention_at
+    rng = np.random.default_rng(seed)
+    b = w.batch - 1
+    rows = np.sort(np.unique(np.concatenate([rng.integers(0, w.seqlen, n_rows - 2),
+                                             [0, w.seqlen - 1]])))
+    H, G = w.heads, w.kv_heads
+    heads = sorted({0, H // 3, (2 * H) // 3, H - 1})
+    idx = torch.as_tensor(rows, device=q.device)
+    eo = el = 0.0
+    for h in heads:
+        g = (h * G) // H
+        kk = k[b:b + 1, :, g:g + 1].float().cpu().numpy()
+        vv = v[b:b + 1, :, g:g + 1].float().cpu().numpy()
+        qr = q[b:b + 1, idx][:, :, h:h + 1].float().cpu().numpy()
+        O, L = attention_at(qr, rows, [0], 1, kk, vv, w.causal)
+        og = o[b:b + 1, idx][:, :, h:h + 1].float().cpu().numpy()
+        lg = lse[b:b + 1, h:h + 1][:, :, idx].cpu().numpy()
+        eo = max(eo, float(np.abs(og - O).max()))
+        el = max(el, float(np.abs(lg - L).max()))
+    return {"rows": int(len(rows)), "heads": heads, "batch": b, "max_abs_o": eo,
+            "max_abs_lse": el, "bars": {"o": 1e-2, "lse": 1e-3}}
+
+
 def tokens_per_s(tflops: float, w) -> float:
     """Tokens/s of the full workload at a given causal-adjusted rate."""
     return tflops * 1e12 / (w.causal_flops() / (w.batch * w.seqlen))
@@ -569,6 +596,8 @@ def run_ours(args, w):
                 cpu["one_core"] = {"value": one[0][0], "unit": "TFLOP/s", "cores": 1,
                                    "sample": f"{one[0][1]} rows, one worker process, "
                                              f"{args.one_core_seconds:.0f} s"}
+            # error maxima of the timed forward's output against the oracle
+            cpu["parity"] = oracle_spot_check(q, k, v, o, lse, w)
 
     if info.is_main:
         line = {

@@ -146,13 +146,13 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
  * of a Grace host).
  * q, k, v, o, lse: host pointers in the shapes of ring_attn_fwd. workspace:
  * device memory of this device, 16-byte aligned, overwritten, of at least two
- * slots (ring_attn_fwd_host_workspace_bytes gives room for eight). copy_stream
+ * slots (ring_attn_fwd_host_workspace_bytes gives room for sixteen). copy_stream
  * may equal stream (the input copies then do not overlap the kernels). */
 ra_status ring_attn_fwd_host(const ra_problem* p, const void* q, const void* k, const void* v,
                              void* o, float* lse, void* workspace, size_t workspace_bytes,
                              void* stream, void* copy_stream);
 
-/* Recommended bytes of device workspace for ring_attn_fwd_host: eight slots (or
+/* Recommended bytes of device workspace for ring_attn_fwd_host: sixteen slots (or
  * one per piece if batch * kv_heads is smaller), a slot being one piece's q, k, v,
  * o, lse, each rounded up to 256 bytes. A piece holds seqlen tokens of
  * heads/kv_heads query heads and one kv head. Any workspace of at least two slots

@@ -144,7 +144,7 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
     if not workspace.is_cuda:
         raise ValueError("workspace must be a CUDA tensor")
     # any workspace of at least two slots works (the library checks the size); the
-    # recommended one, `need` bytes, holds eight
+    # recommended one, `need` bytes, holds sixteen (or one per piece)
     if workspace.device != dev:
         raise ValueError(f"workspace is on {workspace.device}, the call runs on {dev}")
     pin = q.is_pinned()

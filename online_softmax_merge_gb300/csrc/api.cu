@@ -283,9 +283,10 @@ HostSlot host_slot(const ra_problem* pr) {
   return s;
 }
 // Device slots of ring_attn_fwd_host: at least 2 (or one per piece if fewer) are
-// required; the recommended workspace holds kHostSlots, so the input copies can run
-// up to kHostSlots - 1 pieces ahead of the kernels and absorb a stalled copy.
-constexpr int64_t kHostSlots = 8;
+// required; the recommended workspace holds kHostSlots (or one per piece), so the input
+// copies can run up to kHostSlots - 1 pieces ahead of the kernels and absorb copies
+// that stall (tens of milliseconds at a time were seen on the host link).
+constexpr int64_t kHostSlots = 16;
 int64_t host_pieces(const ra_problem* pr) {
   return static_cast<int64_t>(pr->batch) * pr->kv_heads;
 }

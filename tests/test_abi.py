@@ -175,10 +175,10 @@ def test_fwd_host_workspace_and_argument_checks(lib):
     r = lambda x: (x + 255) // 256 * 256
     # a piece: 2 query heads (one kv group) and 1 kv head of one sequence
     slot = r(1000 * 2 * 128 * 2) * 2 + r(1000 * 1 * 128 * 2) * 2 + r(2 * 1000 * 4)
-    # recommended: one slot per piece up to eight (here 3 x 2 = 6 pieces); two suffice
+    # recommended: one slot per piece up to sixteen (here 3 x 2 = 6 pieces); two suffice
     assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr)) == 6 * slot
-    many = _pr(batch=8, seqlen=1000, heads=4, kv_heads=2, head_dim=128, P=4)
-    assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(many)) == 8 * slot
+    many = _pr(batch=12, seqlen=1000, heads=4, kv_heads=2, head_dim=128, P=4)
+    assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(many)) == 16 * slot
     one = _pr(batch=1, seqlen=1000, heads=4, kv_heads=1, head_dim=128, P=4)
     slot1 = r(1000 * 4 * 128 * 2) * 2 + r(1000 * 1 * 128 * 2) * 2 + r(4 * 1000 * 4)
     assert lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(one)) == slot1
