@@ -16,7 +16,10 @@ DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 @pytest.mark.parametrize("N,P", [(8, 4), (12, 3), (4096, 16), (1 << 20, 64), (96, 96)])
 def test_device_shard_map_bit_exact(layout, N, P):
     if layout == "zigzag" and N % (2 * P):
-        pytest.skip("zigzag needs N divisible by 2P")
+        # zigzag needs N divisible by 2P: refused before any launch
+        with pytest.raises(ra.RingAttnError, match="RA_ERR_INVALID_ARG"):
+            ra.shard_map_device(layout, N, P, DEV)
+        return
     own, loc, tok = ra.shard_map_device(layout, N, P, DEV)
     torch.cuda.synchronize()
     if N <= 4096:
