@@ -66,8 +66,21 @@ struct Smem {
 
 enum : int {
   kBarQ = 0, kBarKF = 1, kBarKE = 3, kBarVF = 5, kBarVE = 7, kBarSF = 9, kBarOF = 11,
-  kBarDrain = 13, kBarPF = 14, kNumBars = 18   // kBarPF + 2*i + h: half h of P_i
+  kBarDrain = 13, kBarPF = 14,   // kBarPF + 2*i + h: half h of P_i
+  kBarSB = 18,                   // d = 64: scores ready in score buffer b (3 buffers)
+  kBarPD = 21,                   // d = 64: P V of sub-tile i done (2)
+  kNumBars = 23
 };
+
+// d = 64 keeps three 128-column score buffers (TMEM columns [0,128), [128,256) and
+// [384,512); O0 and O1 take [256,384)) rotating over the sequence k = 2 t + i of
+// (tile t, sub-tile i): scores k go to buffer k mod 3 and are computed three ahead of
+// their P V instead of two, so a sub-tile's next scores are ready when its softmax
+// publishes P. At d = 128 the two O accumulators leave room for two buffers only.
+__device__ __forceinline__ uint32_t score_col(int k) {
+  const int b = k % 3;
+  return b == 2 ? 384u : 128u * static_cast<uint32_t>(b);
+}
 
 struct Unit {
   int bat, g, u;
@@ -190,8 +203,10 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kNumBars + 4);
+  // d = 128 uses the barriers below kBarSB only
+  constexpr int kBars = (D == 64) ? kNumBars : kBarSB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kBars + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8 * i; };
 
   const int warp = threadIdx.x >> 5;
@@ -227,7 +242,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+    for (int i = 0; i < kBars; ++i) mbar_init(bar(i), 1);
     for (int x = 0; x < 4; ++x) mbar_init(bar(kBarPF + x), 4);   // one arrival per softmax warp
     *abort_flag = 0;
     fence_mbar_init();
@@ -307,7 +322,117 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
     // operands); one elected lane issues each group of MMAs and commits. A loop
     // run by a single lane issues MMAs far slower than the tensor core executes
     // them.
-    {
+    if constexpr (D == 64) {
+      // Order: S(0) S(1) S(2), then per tile t: PV(2t), S(2t+3), PV(2t+1), S(2t+4).
+      // S(k+3) reuses the buffer PV(k) has just read; the MMAs of one thread run in
+      // order, so it never overwrites P before its PV has consumed it.
+      const uint32_t tO0 = tmem + L::kOcol, tO1 = tmem + L::kOcol + D;
+      const uint64_t dq0 = smem_desc_sw128(sbase + L::kQ, 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(sbase + L::kQ + L::kTile, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sbase + L::kK, 16, 1024);
+      const uint64_t dk1 = smem_desc_sw128(sbase + L::kK + L::kTile, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sbase + L::kV, L::kChunk, 1024);
+      const uint64_t dv1 = smem_desc_sw128(sbase + L::kV + L::kTile, L::kChunk, 1024);
+      bool ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarQ), 0, p.timeout_ns, abort_flag) &&
+                                        bounded_wait(bar(kBarKF), 0, p.timeout_ns, abort_flag));
+      if (ok) {
+        tc_fence_after_sync();
+        if (elect_one()) {
+          issue_qk<D>(tmem + score_col(0), dq0, dk0);
+          mma_commit(bar(kBarSB + 0));
+          issue_qk<D>(tmem + score_col(1), dq1, dk0);
+          mma_commit(bar(kBarSB + 1));
+          mma_commit(bar(kBarKE + 0));
+        }
+        __syncwarp();
+      }
+      if (ok && T > 1) {
+        ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarKF + 1), 0, p.timeout_ns, abort_flag));
+        if (ok) {
+          tc_fence_after_sync();
+          if (elect_one()) {
+            issue_qk<D>(tmem + score_col(2), dq0, dk1);
+            mma_commit(bar(kBarSB + 2));
+          }
+          __syncwarp();
+        }
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t & 1;
+        const uint32_t ph = static_cast<uint32_t>(t >> 1) & 1;
+        const uint64_t vs = st ? dv1 : dv0;
+        const bool acc = t > 0 || p.load_state;
+        const int k0 = 2 * t, k1 = 2 * t + 1;
+        // P V of sub-tile 0, tile t
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarVF + st), ph, p.timeout_ns, abort_flag) &&
+                                     bounded_wait(bar(kBarPF + 0), t & 1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) issue_pv_half<D>(tO0, tmem + score_col(k0), vs, 0, acc);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 1), t & 1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) {
+          issue_pv_half<D>(tO0, tmem + score_col(k0), vs, 1, acc);
+          mma_commit(bar(kBarPD + 0));
+          if (t + 1 == T) mma_commit(bar(kBarOF + 0));
+          // S of sub-tile 1, tile t + 1 (its K tile already waited for S(2t+2))
+          if (t + 1 < T) {
+            const int st1 = (t + 1) & 1;
+            issue_qk<D>(tmem + score_col(k0 + 3), dq1, st1 ? dk1 : dk0);
+            mma_commit(bar(kBarSB + (k0 + 3) % 3));
+            mma_commit(bar(kBarKE + st1));
+          }
+        }
+        __syncwarp();
+        // P V of sub-tile 1, tile t
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 2), t & 1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) issue_pv_half<D>(tO1, tmem + score_col(k1), vs, 0, acc);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarPF + 3), t & 1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) {
+          issue_pv_half<D>(tO1, tmem + score_col(k1), vs, 1, acc);
+          mma_commit(bar(kBarPD + 1));
+          mma_commit(bar(kBarVE + st));
+          if (t + 1 == T) mma_commit(bar(kBarOF + 1));
+        }
+        __syncwarp();
+        // S of sub-tile 0, tile t + 2
+        if (t + 2 < T) {
+          const int st2 = (t + 2) & 1;
+          const uint32_t ph2 = static_cast<uint32_t>((t + 2) >> 1) & 1;
+          if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarKF + st2), ph2, p.timeout_ns, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          if (elect_one()) {
+            issue_qk<D>(tmem + score_col(k1 + 3), dq0, st2 ? dk1 : dk0);
+            mma_commit(bar(kBarSB + (k1 + 3) % 3));
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok) {
+        if (lane == 0) record_failure(p, abort_flag);
+        if (elect_one()) mma_commit(bar(kBarDrain));
+        __syncwarp();
+        bounded_wait(bar(kBarDrain), 0, kDrainNs, nullptr);
+      }
+    } else {
       const uint32_t tS0 = tmem, tS1 = tmem + 128;
       const uint32_t tO0 = tmem + L::kOcol, tO1 = tmem + L::kOcol + D;
       // Shared-memory descriptors of every tile base, computed once.
@@ -457,7 +582,12 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
         const Seg sk = seg_of(p.layout, p.S, p.P, b, ks);
         const int nk = kv_tiles(p, sk, w.qpos_max);
         for (int kt = 0; kt < nk; ++kt, ++t) {
-          const bool got = bounded_wait(bar(kBarSF + i), t & 1, p.timeout_ns, abort_flag);
+          // this tile's scores: buffer i at d = 128; buffer (2t + i) mod 3 at d = 64
+          const int kseq = 2 * t + i;
+          const uint32_t tSt = (D == 64) ? tmem + score_col(kseq) + lane_off : tS;
+          const bool got =
+              (D == 64) ? bounded_wait(bar(kBarSB + kseq % 3), (kseq / 3) & 1, p.timeout_ns, abort_flag)
+                        : bounded_wait(bar(kBarSF + i), t & 1, p.timeout_ns, abort_flag);
           if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
@@ -466,7 +596,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
           float sc[128];
           {
             uint32_t r[128];
-            tmem_ld_x128(tS, r);
+            tmem_ld_x128(tSt, r);
   #pragma unroll
             for (int j = 0; j < 128; ++j) sc[j] = __uint_as_float(r[j]);
           }
@@ -528,8 +658,21 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(sc[h2 * 64 + 2 * j], sc[h2 * 64 + 2 * j + 1]);
-            tmem_st_x32(tS + h2 * 32, pk);
+            tmem_st_x32(tSt + h2 * 32, pk);
             if (h2 == 0) {
+              // At d = 64 the commit of these scores does not cover the previous
+              // tile's P V of this sub-tile (it was issued after them): wait for it
+              // before touching O. At d = 128 the scores' commit already proves it.
+              if constexpr (D == 64) {
+                if (t > 0) {
+                  const bool pv = bounded_wait(bar(kBarPD + i), (t - 1) & 1, p.timeout_ns, abort_flag);
+                  if (!__all_sync(0xffffffffu, pv)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after_sync();
+                }
+              }
               // Rescale this row's O by alpha before any P V MMA of this tile is
               // issued (the MMA that produced O so far has completed).
               if (__any_sync(0xffffffffu, rescale)) {
@@ -552,6 +695,9 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarPF + 2 * i + h2));
+          }
+          if constexpr (D == 64) {
+            if (!ok) break;
           }
           z_run = z_run * alpha + z_tile;
         }
