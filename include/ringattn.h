@@ -40,8 +40,8 @@
  *  ring_attn_decode_noalloc. `stream` is a cudaStream_t (NULL = legacy default
  *  stream); every call that takes one is asynchronous on it. Calls on one
  *  stream are ordered; the library holds no per-call host state beyond the
- *  ordering events and the output-copy stream that ring_attn_fwd_host creates
- *  and releases itself, so
+ *  ordering events and copy streams that ring_attn_fwd_host creates and releases
+ *  itself, so
  *  concurrent calls on different streams are safe when their output buffers
  *  (and workspaces) do not overlap.
  *
@@ -128,13 +128,16 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
  * The work goes through the GPU in pieces — one sequence's query heads of one
  * kv group with that kv head — in as many device slots as the workspace holds
  * (at least two): while piece i is computed on `stream`, the inputs of the next
- * pieces travel in on `copy_stream` as soon as their slot is free (up to
- * slots - 1 pieces ahead), and the outputs of finished pieces travel out on a
- * stream the call creates and releases itself (strided copies gather a group's
- * heads). Only the first piece's inputs and the last one's outputs are not hidden
- * behind compute, and the slack of the extra slots absorbs a copy that stalls
- * (host-link copies were seen to stall for tens of milliseconds while the GPU
- * changed clocks under its power cap). Each piece is exactly a ring_attn_fwd
+ * pieces travel in as soon as their slot is free (up to slots - 1 pieces ahead),
+ * and the outputs of finished pieces travel out (strided copies gather a group's
+ * heads). A host tensor in page-locked memory that the device maps at the same
+ * address (checked over its whole extent) is moved by the SMs — small copy kernels
+ * on high-priority streams the call creates and releases, whose blocks run ahead of
+ * the ring kernel's; copy-engine transfers over the host link were seen to stall for
+ * tens of milliseconds while the GPU changed clocks under its power cap, SM loads and
+ * stores were not. Other host tensors (pageable memory) go through the copy engines:
+ * inputs on `copy_stream`, outputs on a stream of the call's own. Only the first
+ * piece's inputs and the last one's outputs are not hidden behind compute. Each piece is exactly a ring_attn_fwd
  * call on its heads (the results equal ring_attn_fwd bit for bit). Work enqueued
  * on `stream` before the call happens before any of its copies, and `stream`
  * completes only once the outputs are in host memory, so synchronising `stream`
@@ -146,8 +149,9 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
  * of a Grace host).
  * q, k, v, o, lse: host pointers in the shapes of ring_attn_fwd. workspace:
  * device memory of this device, 16-byte aligned, overwritten, of at least two
- * slots (ring_attn_fwd_host_workspace_bytes gives room for sixteen). copy_stream
- * may equal stream (the input copies then do not overlap the kernels). */
+ * slots (ring_attn_fwd_host_workspace_bytes gives room for sixteen). copy_stream:
+ * the stream of copy-engine input transfers (pageable inputs); it may equal stream
+ * (those transfers then do not overlap the kernels). */
 ra_status ring_attn_fwd_host(const ra_problem* p, const void* q, const void* k, const void* v,
                              void* o, float* lse, void* workspace, size_t workspace_bytes,
                              void* stream, void* copy_stream);

@@ -290,6 +290,24 @@ constexpr int64_t kHostSlots = 16;
 int64_t host_pieces(const ra_problem* pr) {
   return static_cast<int64_t>(pr->batch) * pr->kv_heads;
 }
+// True when [p, p + bytes) is page-locked host memory that this device reaches at the
+// same address (checked at its first and last byte), so that kernels may read or
+// write it directly; false for pageable memory or anything else (copy engines then).
+bool mapped_host(const void* p, size_t bytes) {
+  if (bytes == 0 || (reinterpret_cast<uintptr_t>(p) & 3u)) return false;
+  const char* ends[2] = {static_cast<const char*>(p), static_cast<const char*>(p) + bytes - 1};
+  for (const char* e : ends) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, e) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer != static_cast<const void*>(e))
+      return false;
+  }
+  return true;
+}
+
 size_t fwd_host_min_workspace(const ra_problem* pr) {
   const int64_t n = host_pieces(pr);
   return host_slot(pr).total * static_cast<size_t>(n < 2 ? n : 2);
@@ -344,7 +362,6 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   if ((st = current_device(&d)) != RA_OK) return st;
   if ((st = resident(d, {workspace})) != RA_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);        // kernels
-  const cudaStream_t is = static_cast<cudaStream_t>(copy_stream);   // inputs in
   const HostSlot hs = host_slot(pr);
   const int B = pr->batch, G = pr->kv_heads, H = pr->heads, N = pr->seqlen, D = pr->head_dim;
   const int hpg = H / G;
@@ -367,16 +384,35 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   const size_t w_q = static_cast<size_t>(hpg) * D * 2;      // a piece's bytes per token
   const size_t w_kv = static_cast<size_t>(D) * 2;
   const size_t lse_piece = static_cast<size_t>(hpg) * N * sizeof(float);
-  // Outputs leave on a stream of this call's own, so a stalled output copy never
-  // holds up the input copies (and the reverse).
-  cudaStream_t os = nullptr;
-  cudaError_t e = cudaStreamCreateWithFlags(&os, cudaStreamNonBlocking);
+  // Tensors in page-locked memory mapped at the same address are moved by copy kernels
+  // (hostcopy.cu); the rest by the copy engines.
+  const size_t bq = static_cast<size_t>(B) * N * row_q, bkv = static_cast<size_t>(B) * N * row_kv;
+  const bool zq = mapped_host(q, bq), zk = mapped_host(k, bkv), zv = mapped_host(v, bkv);
+  const bool zo = mapped_host(o, bq), zl = mapped_host(lse, static_cast<size_t>(B) * G * lse_piece);
+  // Outputs leave on a stream of this call's own, so a stalled output copy never holds
+  // up the inputs (and the reverse); inputs come in on another stream of its own when
+  // copy kernels move any of them, else on copy_stream. Streams of copy kernels run at
+  // the device's highest priority, so their blocks go ahead of the ring kernel's.
+  int lo_prio = 0, hi_prio = 0;
+  cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio);
   if (e != cudaSuccess) return RA_ERR_CUDA;
+  cudaStream_t os = nullptr, own_is = nullptr;
+  e = cudaStreamCreateWithPriority(&os, cudaStreamNonBlocking, hi_prio);
+  if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (zq || zk || zv) {
+    e = cudaStreamCreateWithPriority(&own_is, cudaStreamNonBlocking, hi_prio);
+    if (e != cudaSuccess) {
+      cudaStreamDestroy(os);
+      return RA_ERR_CUDA;
+    }
+  }
+  const cudaStream_t is = own_is ? own_is : static_cast<cudaStream_t>(copy_stream);
   // events: start, inputs-done joined back, end; per piece: inputs in, kernel done, outputs out
   const int n_ev = 3 + 3 * n;
   cudaEvent_t* ev = new (std::nothrow) cudaEvent_t[n_ev];
   if (ev == nullptr) {
     cudaStreamDestroy(os);
+    if (own_is) cudaStreamDestroy(own_is);
     return RA_ERR_CUDA;
   }
   int made = 0;
@@ -394,12 +430,13 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
     const uint8_t* qs = static_cast<const uint8_t*>(q) + static_cast<size_t>(b) * N * row_q + g * w_q;
     const uint8_t* ks = static_cast<const uint8_t*>(k) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
     const uint8_t* vs = static_cast<const uint8_t*>(v) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
-    cudaError_t r = cudaMemcpy2DAsync(s0, w_q, qs, row_q, w_q, N, cudaMemcpyHostToDevice, is);
-    if (r == cudaSuccess)
-      r = cudaMemcpy2DAsync(s0 + hs.q, w_kv, ks, row_kv, w_kv, N, cudaMemcpyHostToDevice, is);
-    if (r == cudaSuccess)
-      r = cudaMemcpy2DAsync(s0 + hs.q + hs.kv, w_kv, vs, row_kv, w_kv, N, cudaMemcpyHostToDevice,
-                            is);
+    auto in = [&](bool kernel, void* dst, const void* src, size_t pitch, size_t width) {
+      return kernel ? launch_rows_copy(dst, width, src, pitch, width, N, is)
+                    : cudaMemcpy2DAsync(dst, width, src, pitch, width, N, cudaMemcpyHostToDevice, is);
+    };
+    cudaError_t r = in(zq, s0, qs, row_q, w_q);
+    if (r == cudaSuccess) r = in(zk, s0 + hs.q, ks, row_kv, w_kv);
+    if (r == cudaSuccess) r = in(zv, s0 + hs.q + hs.kv, vs, row_kv, w_kv);
     if (r == cudaSuccess) r = cudaEventRecord(ev_in(i), is);
     return r;
   };
@@ -421,12 +458,15 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
     e = cudaEventRecord(ev_k(i), cs);
     // outputs of piece i out once its kernel is done
     if (e == cudaSuccess) e = cudaStreamWaitEvent(os, ev_k(i), 0);
+    uint8_t* od = static_cast<uint8_t*>(o) + static_cast<size_t>(b) * N * row_q + g * w_q;
+    // lse [B, H, N]: the group's heads are consecutive rows
+    uint8_t* ld = reinterpret_cast<uint8_t*>(lse) + (static_cast<size_t>(b) * G + g) * lse_piece;
     if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(static_cast<uint8_t*>(o) + static_cast<size_t>(b) * N * row_q + g * w_q, row_q, p.o, w_q, w_q,
-                            N, cudaMemcpyDeviceToHost, os);
-    if (e == cudaSuccess)   // lse [B, H, N]: the group's heads are consecutive rows
-      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + (static_cast<size_t>(b) * G + g) * lse_piece,
-                          p.lse, lse_piece, cudaMemcpyDeviceToHost, os);
+      e = zo ? launch_rows_copy(od, row_q, p.o, w_q, w_q, N, os)
+             : cudaMemcpy2DAsync(od, row_q, p.o, w_q, w_q, N, cudaMemcpyDeviceToHost, os);
+    if (e == cudaSuccess)
+      e = zl ? launch_rows_copy(ld, lse_piece, p.lse, lse_piece, lse_piece, 1, os)
+             : cudaMemcpyAsync(ld, p.lse, lse_piece, cudaMemcpyDeviceToHost, os);
     if (e == cudaSuccess) e = cudaEventRecord(ev_out(i), os);
     // the slot is free once its outputs are out (its inputs were consumed before):
     // the inputs of piece i + S come in there
@@ -445,6 +485,7 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);   // released once they complete
   delete[] ev;
   cudaStreamDestroy(os);                                      // likewise
+  if (own_is) cudaStreamDestroy(own_is);
   if (st != RA_OK) return st;
   return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }

@@ -80,3 +80,42 @@ def test_host_forward_with_fewer_slots_than_pieces(slots):
     torch.cuda.synchronize()
     assert torch.equal(o_h, o_d.cpu())
     assert torch.equal(l_h, l_d.cpu())
+
+
+@pytest.mark.parametrize("pinned", [(True, False, True, False, True), (False, True, False, True, False)])
+def test_host_forward_with_mixed_page_locked_and_pageable_tensors(pinned):
+    """Each host tensor goes its own way: page-locked ones through the SMs' copy
+    kernels, pageable ones through the copy engines; the results are the same."""
+    w = Workload("hostmix", 2, 4 * 200, 4, 2, 128, 4, "striped", True, 440)
+    q, k, v = make_qkv(w)
+    pq, pk, pv, po, pl = pinned
+    q, k, v = (t.pin_memory() if p else t for t, p in ((q, pq), (k, pk), (v, pv)))
+    o_h = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=po)
+    l_h = torch.empty((w.batch, w.heads, w.seqlen), dtype=torch.float32, pin_memory=pl)
+    ra.fwd_host(q, k, v, w.P, w.layout, w.causal, out=o_h, lse=l_h, device=DEV)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    o_d, l_d = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())
+
+
+def test_host_forward_on_views_inside_page_locked_buffers():
+    """Tensors that start inside a larger page-locked allocation (not at its base)."""
+    w = Workload("hostview", 1, 4 * 150, 4, 2, 64, 4, "contiguous", True, 450)
+    q, k, v = make_qkv(w)
+    big = torch.empty(q.numel() + 2 * k.numel() + 3 * 1024, dtype=torch.bfloat16).pin_memory()
+    qv = big[1024:1024 + q.numel()].view(q.shape)
+    kv_ = big[2048 + q.numel():2048 + q.numel() + k.numel()].view(k.shape)
+    vv = big[3072 + q.numel() + k.numel():3072 + q.numel() + 2 * k.numel()].view(v.shape)
+    qv.copy_(q)
+    kv_.copy_(k)
+    vv.copy_(v)
+    o_h, l_h = ra.fwd_host(qv, kv_, vv, w.P, w.layout, w.causal, device=DEV)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    o_d, l_d = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())
