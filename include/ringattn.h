@@ -318,7 +318,9 @@ ra_status ring_attn_selftest_timeout(uint64_t limit_ns, void* stream);
  * of the ring, step, backward and decode kernels first checks its index range
  * against its buffer; a failed check records RA_ERR_BOUNDS in the status word and
  * skips the access. (The merge, finalize and index-map kernels address memory only
- * through their launch coordinates under explicit guards and carry no checks.)
+ * through their launch coordinates under explicit guards, and the host-copy kernels
+ * of ring_attn_fwd_host only within ranges the host has checked; they carry no
+ * checks.)
  * Results are otherwise those of the release build. No counterpart in the pages. */
 int32_t ring_attn_debug_checks(void);
 
