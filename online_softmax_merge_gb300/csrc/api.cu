@@ -424,14 +424,18 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   auto ev_k = [&](int i) { return ev[3 + n + i]; };
   auto ev_out = [&](int i) { return ev[3 + 2 * n + i]; };
   auto slot = [&](int i) { return static_cast<uint8_t*>(workspace) + (i % S) * hs.total; };
+  // Copy kernels use one block per SM while ring kernels share the GPU, four when the
+  // first piece's inputs or the last piece's outputs move with nothing else running.
+  constexpr int kCopyBlocks = 152, kCopyBlocksAlone = 4 * 152;
   auto h2d = [&](int i) -> cudaError_t {
     const int b = i / G, g = i % G;
+    const int blocks = i == 0 ? kCopyBlocksAlone : kCopyBlocks;
     uint8_t* s0 = slot(i);
     const uint8_t* qs = static_cast<const uint8_t*>(q) + static_cast<size_t>(b) * N * row_q + g * w_q;
     const uint8_t* ks = static_cast<const uint8_t*>(k) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
     const uint8_t* vs = static_cast<const uint8_t*>(v) + static_cast<size_t>(b) * N * row_kv + g * w_kv;
     auto in = [&](bool kernel, void* dst, const void* src, size_t pitch, size_t width) {
-      return kernel ? launch_rows_copy(dst, width, src, pitch, width, N, is)
+      return kernel ? launch_rows_copy(dst, width, src, pitch, width, N, blocks, is)
                     : cudaMemcpy2DAsync(dst, width, src, pitch, width, N, cudaMemcpyHostToDevice, is);
     };
     cudaError_t r = in(zq, s0, qs, row_q, w_q);
@@ -461,11 +465,12 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
     uint8_t* od = static_cast<uint8_t*>(o) + static_cast<size_t>(b) * N * row_q + g * w_q;
     // lse [B, H, N]: the group's heads are consecutive rows
     uint8_t* ld = reinterpret_cast<uint8_t*>(lse) + (static_cast<size_t>(b) * G + g) * lse_piece;
+    const int oblocks = i + 1 == n ? kCopyBlocksAlone : kCopyBlocks;
     if (e == cudaSuccess)
-      e = zo ? launch_rows_copy(od, row_q, p.o, w_q, w_q, N, os)
+      e = zo ? launch_rows_copy(od, row_q, p.o, w_q, w_q, N, oblocks, os)
              : cudaMemcpy2DAsync(od, row_q, p.o, w_q, w_q, N, cudaMemcpyDeviceToHost, os);
     if (e == cudaSuccess)
-      e = zl ? launch_rows_copy(ld, lse_piece, p.lse, lse_piece, lse_piece, 1, os)
+      e = zl ? launch_rows_copy(ld, lse_piece, p.lse, lse_piece, lse_piece, 1, oblocks, os)
              : cudaMemcpyAsync(ld, p.lse, lse_piece, cudaMemcpyDeviceToHost, os);
     if (e == cudaSuccess) e = cudaEventRecord(ev_out(i), os);
     // the slot is free once its outputs are out (its inputs were consumed before):

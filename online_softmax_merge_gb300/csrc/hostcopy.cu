@@ -19,7 +19,6 @@ namespace ra {
 namespace {
 
 constexpr int kCopyThreads = 256;
-constexpr int kCopyBlocks = 152;   // one per SM of a GB300
 
 // dst[r * dpitch + c] = src[r * spitch + c] for r < rows, c < width (in elements of T)
 template <typename T>
@@ -39,10 +38,11 @@ bool multiple(uintptr_t x, uintptr_t m) { return x % m == 0; }
 }  // namespace
 
 // Copies rows x width bytes from src (row pitch spitch) to dst (row pitch dpitch) with
-// the SMs; 16-byte elements when every address and size allows, else 4-byte ones.
-// Returns cudaErrorInvalidValue (nothing launched) when not even 4 bytes divide them.
+// the SMs, in `blocks` blocks; 16-byte elements when every address and size allows,
+// else 4-byte ones. Returns cudaErrorInvalidValue (nothing launched) when not even 4
+// bytes divide them.
 cudaError_t launch_rows_copy(void* dst, size_t dpitch, const void* src, size_t spitch,
-                             size_t width, size_t rows, cudaStream_t st) {
+                             size_t width, size_t rows, int blocks, cudaStream_t st) {
   static bool carveout_done = false;
   if (!carveout_done) {
     // no shared memory: prefer the split that lets these blocks sit beside others
@@ -56,12 +56,12 @@ cudaError_t launch_rows_copy(void* dst, size_t dpitch, const void* src, size_t s
                       static_cast<uintptr_t>(width);
   if (rows == 0 || width == 0) return cudaSuccess;
   if (multiple(a, 16)) {
-    rows_copy<uint4><<<kCopyBlocks, kCopyThreads, 0, st>>>(
+    rows_copy<uint4><<<blocks, kCopyThreads, 0, st>>>(
         static_cast<uint4*>(dst), static_cast<const uint4*>(src), static_cast<long long>(rows),
         static_cast<long long>(width / 16), static_cast<long long>(spitch / 16),
         static_cast<long long>(dpitch / 16));
   } else if (multiple(a, 4)) {
-    rows_copy<uint32_t><<<kCopyBlocks, kCopyThreads, 0, st>>>(
+    rows_copy<uint32_t><<<blocks, kCopyThreads, 0, st>>>(
         static_cast<uint32_t*>(dst), static_cast<const uint32_t*>(src),
         static_cast<long long>(rows), static_cast<long long>(width / 4),
         static_cast<long long>(spitch / 4), static_cast<long long>(dpitch / 4));

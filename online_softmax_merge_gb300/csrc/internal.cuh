@@ -118,9 +118,10 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t
 cudaError_t launch_selftest_bounds(int* status, cudaStream_t st);
 
 // rows x width bytes from src (row pitch spitch) to dst (row pitch dpitch), copied by
-// the SMs (hostcopy.cu); either side may be mapped page-locked host memory.
+// the SMs in `blocks` blocks (hostcopy.cu); either side may be mapped page-locked host
+// memory.
 cudaError_t launch_rows_copy(void* dst, size_t dpitch, const void* src, size_t spitch,
-                             size_t width, size_t rows, cudaStream_t st);
+                             size_t width, size_t rows, int blocks, cudaStream_t st);
 // Pass-Q decode, phase 1: per-(shard segment, key chunk) partials into the
 // workspace. tk, tv: [B,N,G,d] views with 32-row boxes.
 cudaError_t launch_decode_partials(const RingParams& p, const CUtensorMap& tk,
