@@ -424,9 +424,11 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   auto ev_k = [&](int i) { return ev[3 + n + i]; };
   auto ev_out = [&](int i) { return ev[3 + 2 * n + i]; };
   auto slot = [&](int i) { return static_cast<uint8_t*>(workspace) + (i % S) * hs.total; };
-  // Copy kernels use one block per SM while ring kernels share the GPU, four when the
-  // first piece's inputs or the last piece's outputs move with nothing else running.
-  constexpr int kCopyBlocks = 152, kCopyBlocksAlone = 4 * 152;
+  // Copy kernels run 38 blocks (a quarter of the SMs) while ring kernels share the GPU:
+  // they have slack and fewer blocks take fewer SM slots from the ring kernel; four
+  // blocks per SM when the first piece's inputs or the last piece's outputs move with
+  // nothing else running.
+  constexpr int kCopyBlocks = 38, kCopyBlocksAlone = 4 * 152;
   auto h2d = [&](int i) -> cudaError_t {
     const int b = i / G, g = i % G;
     const int blocks = i == 0 ? kCopyBlocksAlone : kCopyBlocks;
