@@ -131,7 +131,7 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
  * pieces travel in as soon as their slot is free (up to slots - 1 pieces ahead),
  * and the outputs of finished pieces travel out (strided copies gather a group's
  * heads). A host tensor in page-locked memory that the device maps at the same
- * address (checked over its whole extent) is moved by the SMs — small copy kernels
+ * address (ring_attn_host_mapped) is moved by the SMs — small copy kernels
  * on high-priority streams the call creates and releases, whose blocks run ahead of
  * the ring kernel's; copy-engine transfers over the host link were seen to stall for
  * tens of milliseconds while the GPU changed clocks under its power cap, SM loads and
@@ -155,6 +155,16 @@ ra_status ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const
 ra_status ring_attn_fwd_host(const ra_problem* p, const void* q, const void* k, const void* v,
                              void* o, float* lse, void* workspace, size_t workspace_bytes,
                              void* stream, void* copy_stream);
+
+/* 1 when ring_attn_fwd_host would move the host range [p, p + bytes) with copy
+ * kernels: page-locked memory that the current device maps at the same address,
+ * 4-byte aligned, with the whole range inside one allocation or registration (its
+ * first and last byte checked, then the extent of the allocation that holds p).
+ * 0 otherwise — pageable memory, device memory, a range that runs past the end of
+ * its allocation, a null pointer, bytes == 0, or a device that is not sm_103 — and
+ * such a tensor goes through the copy engines. A pure query: nothing is launched
+ * and no memory is touched. No counterpart in the pages. */
+int32_t ring_attn_host_mapped(const void* p, size_t bytes);
 
 /* Recommended bytes of device workspace for ring_attn_fwd_host: sixteen slots (or
  * one per piece if batch * kv_heads is smaller), a slot being one piece's q, k, v,

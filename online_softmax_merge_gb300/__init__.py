@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import (LAYOUTS, RA_ERR_BOUNDS, RA_ERR_CUDA, RA_ERR_INVALID_ARG,  # noqa: F401
                    RA_ERR_TIMEOUT, RA_ERR_UNSUPPORTED, RA_OK, TILE, RingAttnError, check, load)
 
-__all__ = ["fwd", "fwd_host", "fwd_host_workspace_bytes", "bwd", "bwd_workspace_bytes", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
+__all__ = ["fwd", "fwd_host", "fwd_host_workspace_bytes", "host_mapped", "bwd", "bwd_workspace_bytes", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
            "tile_classes", "mask", "last_error", "selftest_timeout", "selftest_bounds",
            "debug_checks", "problem", "RingAttnError",
            "empty_state", "LAYOUTS", "TILE"]
@@ -165,6 +165,19 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
             ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream(dev),
             ctypes.c_void_p(copy_stream.cuda_stream)))
     return out, lse
+
+
+def host_mapped(t: torch.Tensor, device=None) -> bool:
+    """Whether ring_attn_fwd_host moves host tensor `t` (its whole storage extent
+    from its first element) with copy kernels rather than the copy engines
+    (ring_attn_host_mapped): page-locked memory that `device` (default: the current
+    CUDA device) maps at the same address, inside one allocation."""
+    lib = load()
+    if t.device.type != "cpu":
+        raise ValueError("host_mapped takes a CPU tensor")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return bool(lib.ring_attn_host_mapped(_ptr(t), ctypes.c_size_t(t.numel() * t.element_size())))
 
 
 def bwd_workspace_bytes(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int,

@@ -34,6 +34,7 @@ SIGNATURES = {
     "ring_attn_fwd": (_i32, [_PP, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ring_attn_fwd_host": (_i32, [_PP, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]),
     "ring_attn_fwd_host_workspace_bytes": (ctypes.c_size_t, [_PP]),
+    "ring_attn_host_mapped": (_i32, [_vp, ctypes.c_size_t]),
     "ring_attn_step": (_i32, [_PP, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ring_attn_step_simt": (_i32, [_PP, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "ring_attn_finalize": (_i32, [_PP, _vp, _vp, _vp, _vp, _vp, _vp]),

@@ -290,9 +290,28 @@ constexpr int64_t kHostSlots = 16;
 int64_t host_pieces(const ra_problem* pr) {
   return static_cast<int64_t>(pr->batch) * pr->kv_heads;
 }
+typedef CUresult (*PointerAttrFn)(void*, CUpointer_attribute, CUdeviceptr);
+
+PointerAttrFn pointer_attr_fn() {
+  static PointerAttrFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PointerAttrFn>(ptr);
+  });
+  return fn;
+}
+
 // True when [p, p + bytes) is page-locked host memory that this device reaches at the
-// same address (checked at its first and last byte), so that kernels may read or
-// write it directly; false for pageable memory or anything else (copy engines then).
+// same address, so that kernels may read or write it directly: its first and last
+// byte are such memory, and one allocation (or registration) holds the whole range,
+// so no byte between them is unmapped. False for pageable memory, for ranges that
+// run over the end of their allocation, and whenever a query fails (the copy engines
+// then move the tensor).
 bool mapped_host(const void* p, size_t bytes) {
   if (bytes == 0 || (reinterpret_cast<uintptr_t>(p) & 3u)) return false;
   const char* ends[2] = {static_cast<const char*>(p), static_cast<const char*>(p) + bytes - 1};
@@ -305,7 +324,15 @@ bool mapped_host(const void* p, size_t bytes) {
     if (a.type != cudaMemoryTypeHost || a.devicePointer != static_cast<const void*>(e))
       return false;
   }
-  return true;
+  PointerAttrFn fn = pointer_attr_fn();
+  if (fn == nullptr) return false;
+  CUdeviceptr start = 0;
+  size_t size = 0;
+  const CUdeviceptr at = static_cast<CUdeviceptr>(reinterpret_cast<uintptr_t>(p));
+  if (fn(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, at) != CUDA_SUCCESS ||
+      fn(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, at) != CUDA_SUCCESS)
+    return false;
+  return at >= start && at - start <= size && bytes <= size - (at - start);
 }
 
 size_t fwd_host_min_workspace(const ra_problem* pr) {
@@ -495,6 +522,12 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   if (own_is) cudaStreamDestroy(own_is);
   if (st != RA_OK) return st;
   return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+int32_t ring_attn_host_mapped(const void* p, size_t bytes) {
+  DevInfo* d = nullptr;
+  if (p == nullptr || current_device(&d) != RA_OK) return 0;
+  return mapped_host(p, bytes) ? 1 : 0;
 }
 
 ra_status ring_attn_step(const ra_problem* pr, int32_t s, int32_t first, const void* q,
@@ -783,7 +816,7 @@ const char* ra_status_str(ra_status s) {
   return "RA_ERR_UNKNOWN";
 }
 
-int32_t ring_attn_version(void) { return 100; }
+int32_t ring_attn_version(void) { return 101; }
 
 int32_t ring_attn_debug_checks(void) { return kDebugChecks ? 1 : 0; }
 

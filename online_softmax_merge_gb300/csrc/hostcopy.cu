@@ -13,6 +13,8 @@
 // kernels address only rows [0, rows) x bytes [0, width) of each side.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "internal.cuh"
 
 namespace ra {
@@ -43,13 +45,18 @@ bool multiple(uintptr_t x, uintptr_t m) { return x % m == 0; }
 // bytes divide them.
 cudaError_t launch_rows_copy(void* dst, size_t dpitch, const void* src, size_t spitch,
                              size_t width, size_t rows, int blocks, cudaStream_t st) {
-  static bool carveout_done = false;
-  if (!carveout_done) {
-    // no shared memory: prefer the split that lets these blocks sit beside others
-    cudaFuncSetAttribute(rows_copy<uint4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(rows_copy<uint32_t>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         100);
-    carveout_done = true;
+  // No shared memory: prefer the split that lets these blocks sit beside others. A
+  // preference only, set once per device (one bit per ordinal; callers may be threads).
+  static std::atomic<unsigned long long> carveout_done{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(carveout_done.load() & bit)) {
+      cudaFuncSetAttribute(rows_copy<uint4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      cudaFuncSetAttribute(rows_copy<uint32_t>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           100);
+      carveout_done.fetch_or(bit);
+    }
   }
   const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) |
                       static_cast<uintptr_t>(dpitch) | static_cast<uintptr_t>(spitch) |

@@ -34,7 +34,7 @@ def test_header_declarations_match_binding():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name
-    assert lib.ring_attn_version() == 100
+    assert lib.ring_attn_version() == 101
 
 
 def test_debug_build_exports_the_same_symbols_and_reports_its_checks(lib):
@@ -193,3 +193,12 @@ def test_fwd_host_workspace_and_argument_checks(lib):
         bad[i] = None
         assert lib.ring_attn_fwd_host(ctypes.byref(pr), *bad, FAKE, 2 * slot, None, None) == \
             _lib.RA_ERR_INVALID_ARG
+
+
+def test_host_mapped_refuses_pageable_null_and_empty_ranges(lib):
+    """Pageable memory, a null pointer and an empty range read 0, with or without a
+    device (without one every range reads 0); the query launches nothing."""
+    buf = ctypes.create_string_buffer(4096)
+    assert lib.ring_attn_host_mapped(ctypes.addressof(buf), 4096) == 0
+    assert lib.ring_attn_host_mapped(None, 4096) == 0
+    assert lib.ring_attn_host_mapped(ctypes.addressof(buf), 0) == 0

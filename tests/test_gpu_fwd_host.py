@@ -119,3 +119,46 @@ def test_host_forward_on_views_inside_page_locked_buffers():
     torch.cuda.synchronize()
     assert torch.equal(o_h, o_d.cpu())
     assert torch.equal(l_h, l_d.cpu())
+
+
+def test_host_mapped_sees_page_locked_memory_and_views_inside_it():
+    """The query behind the choice between copy kernels and copy engines."""
+    pinned = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
+    assert ra.host_mapped(pinned, DEV)
+    assert ra.host_mapped(pinned[4096:8192], DEV)
+    assert not ra.host_mapped(torch.empty(1 << 20, dtype=torch.uint8), DEV)
+    with pytest.raises(ValueError):
+        ra.host_mapped(pinned.to(DEV), DEV)
+    lib = ra.load()
+    assert lib.ring_attn_host_mapped(None, 16) == 0
+    assert lib.ring_attn_host_mapped(pinned.data_ptr(), 0) == 0
+    assert lib.ring_attn_host_mapped(pinned.data_ptr() + 1, 16) == 0      # not 4-byte aligned
+
+
+def test_host_mapped_refuses_a_range_with_an_unmapped_hole():
+    """Two registered 2 MiB ranges of one pageable buffer with 2 MiB between them:
+    the first and last byte of the span are mapped, its middle is not, so the span
+    must go through the copy engines. Only registers memory and queries attributes."""
+    MB = 1 << 20
+    buf = torch.empty(9 * MB, dtype=torch.uint8)
+    off = (-buf.data_ptr()) % MB
+    a0 = buf.data_ptr() + off
+    cr = torch.cuda.cudart()
+    flags = 3   # cudaHostRegisterPortable | cudaHostRegisterMapped
+    torch.cuda.synchronize(DEV)
+    r1 = int(cr.cudaHostRegister(a0, 2 * MB, flags))
+    r2 = int(cr.cudaHostRegister(a0 + 4 * MB, 2 * MB, flags)) if r1 == 0 else -1
+    try:
+        if r1 != 0 or r2 != 0:
+            pytest.skip(f"cudaHostRegister returned {r1}, {r2}")
+        first, second = buf[off:off + 2 * MB], buf[off + 4 * MB:off + 6 * MB]
+        if not (ra.host_mapped(first, DEV) and ra.host_mapped(second, DEV)):
+            pytest.skip("registered memory is not mapped at its host address on this device")
+        assert not ra.host_mapped(buf[off:off + 6 * MB], DEV)
+        assert not ra.host_mapped(buf[off + MB:off + 5 * MB], DEV)
+        assert not ra.host_mapped(buf[off:off + 2 * MB + 4096], DEV)     # runs past the end
+    finally:
+        if r1 == 0:
+            cr.cudaHostUnregister(a0)
+        if r2 == 0:
+            cr.cudaHostUnregister(a0 + 4 * MB)
