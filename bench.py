@@ -520,7 +520,7 @@ def run_ours(args, w):
                   "launches_per_call": 2,
                   "workload": f"1 query token per sequence at position N-1 against the {w.name} "
                               f"KV cache (B={w.batch}, N={w.seqlen}, G={w.kv_heads}, d={w.head_dim}, "
-                              f"P={w.P} {w.layout}); partials per (shard, 4096-key chunk) + merge"}
+                              f"P={w.P} {w.layout}); partials per (shard, chunk of up to 8192 keys) + merge"}
         del qd, ws, od, ld
 
     # ---- the same forward composed from the step API: P ring_attn_step calls with the
