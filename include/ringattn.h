@@ -51,6 +51,12 @@
  *  ring_attn_last_error — may be captured into a graph; a replay computes what
  *  the eager call would on the buffers' contents at replay time.
  *
+ *  Outputs, in/out state and workspaces must not overlap one another or any
+ *  input (inputs may overlap each other, e.g. the same tensor passed as k and
+ *  v): a call whose written ranges would share a byte with another argument's
+ *  range, counted from the shapes above, returns RA_ERR_INVALID_ARG. There is no
+ *  in-place form.
+ *
  *  Errors: argument errors are returned synchronously before any launch and
  *  nothing is written. Every device pointer is checked to be memory the current
  *  device's kernels may touch (its device memory — cudaMalloc, pools, virtual-memory
@@ -73,7 +79,8 @@ extern "C" {
 typedef enum {
   RA_OK = 0,
   RA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, N % P != 0, H % G != 0, misaligned,
-                               or a device pointer that is not memory of the current device */
+                               a written range overlapping another argument, or a device
+                               pointer that is not memory of the current device */
   RA_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, no sm_103a device, or a size past a
                                launch limit (e.g. batch x heads x P x query tiles >= 2^31) */
   RA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */

@@ -57,6 +57,46 @@ ra_status current_device(DevInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The bytes [p, p + bytes) an argument covers.
+struct Span {
+  const void* p;
+  size_t bytes;
+};
+
+bool overlap(const Span& a, const Span& b) {
+  if (a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a.p), y = reinterpret_cast<uintptr_t>(b.p);
+  return x < y + b.bytes && y < x + a.bytes;
+}
+
+// True when no range a call writes shares a byte with another written range or with a
+// range it reads. Read ranges may overlap each other (the same tensor passed twice);
+// a kernel writing where other CTAs still read would give undefined results.
+bool writes_disjoint(std::initializer_list<Span> writes, std::initializer_list<Span> reads) {
+  for (const Span* w = writes.begin(); w != writes.end(); ++w) {
+    for (const Span& r : reads)
+      if (overlap(*w, r)) return false;
+    for (const Span* w2 = w + 1; w2 != writes.end(); ++w2)
+      if (overlap(*w, *w2)) return false;
+  }
+  return true;
+}
+
+// Bytes of the tensors of a problem: q and o, k and v, one [B, H, N] fp32 row set
+// (lse, m, z), and y.
+struct Bytes {
+  size_t q, kv, rows, y;
+};
+Bytes tensor_bytes(const ra_problem* pr) {
+  const size_t tok = static_cast<size_t>(pr->batch) * static_cast<size_t>(pr->seqlen);
+  Bytes b;
+  b.q = tok * pr->heads * pr->head_dim * 2;
+  b.kv = tok * pr->kv_heads * pr->head_dim * 2;
+  b.rows = tok * pr->heads * sizeof(float);
+  b.y = tok * pr->heads * pr->head_dim * sizeof(float);
+  return b;
+}
+
 // Memory the kernels launched on the current device may touch: device memory of that
 // device (cudaMalloc, stream-ordered pools, virtual-memory mappings) or managed memory.
 // Host memory (pageable or pinned) and other devices' memory are refused before
@@ -226,6 +266,9 @@ ra_status check_step_args(const ra_problem* pr, int32_t s, const void* q, const 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(m) || !aligned16(z) ||
       !aligned16(y))
     return RA_ERR_INVALID_ARG;
+  const Bytes b = tensor_bytes(pr);
+  if (!writes_disjoint({{m, b.rows}, {z, b.rows}, {y, b.y}}, {{q, b.q}, {k, b.kv}, {v, b.kv}}))
+    return RA_ERR_INVALID_ARG;
   return RA_OK;
 }
 
@@ -355,6 +398,9 @@ ra_status ring_attn_fwd(const ra_problem* pr, const void* q, const void* k, cons
   if (!q || !k || !v || !o || !lse) return RA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return RA_ERR_INVALID_ARG;
+  const Bytes b = tensor_bytes(pr);
+  if (!writes_disjoint({{o, b.q}, {lse, b.rows}}, {{q, b.q}, {k, b.kv}, {v, b.kv}}))
+    return RA_ERR_INVALID_ARG;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
   if ((st = resident(d, {q, k, v, o, lse})) != RA_OK) return st;
@@ -384,6 +430,12 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   if (!q || !k || !v || !o || !lse || !workspace || !aligned16(workspace))
     return RA_ERR_INVALID_ARG;
   if (workspace_bytes < fwd_host_min_workspace(pr)) return RA_ERR_INVALID_ARG;
+  {
+    const Bytes b = tensor_bytes(pr);
+    if (!writes_disjoint({{o, b.q}, {lse, b.rows}, {workspace, workspace_bytes}},
+                         {{q, b.q}, {k, b.kv}, {v, b.kv}}))
+      return RA_ERR_INVALID_ARG;
+  }
   if (host_pieces(pr) > (1 << 24)) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
@@ -587,6 +639,9 @@ ra_status ring_attn_finalize(const ra_problem* pr, const float* m, const float* 
   if (!m || !z || !y || !o || !lse) return RA_ERR_INVALID_ARG;
   if (!aligned16(m) || !aligned16(z) || !aligned16(y) || !aligned16(o) || !aligned16(lse))
     return RA_ERR_INVALID_ARG;
+  const Bytes b = tensor_bytes(pr);
+  if (!writes_disjoint({{o, b.q}, {lse, b.rows}}, {{m, b.rows}, {z, b.rows}, {y, b.y}}))
+    return RA_ERR_INVALID_ARG;
   if (static_cast<long long>(pr->batch) > 65535 || pr->heads > 65535) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
@@ -612,6 +667,14 @@ ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_
   if (!o_parts || !lse_parts || !o || !lse) return RA_ERR_INVALID_ARG;
   if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse))
     return RA_ERR_INVALID_ARG;
+  {
+    const size_t rows = static_cast<size_t>(batch) * seqlen * heads;
+    const size_t n = static_cast<size_t>(n_parts);
+    if (!writes_disjoint({{o, rows * head_dim * 2}, {lse, rows * sizeof(float)}},
+                         {{o_parts, n * rows * head_dim * sizeof(float)},
+                          {lse_parts, n * rows * sizeof(float)}}))
+      return RA_ERR_INVALID_ARG;
+  }
   DevInfo* d = nullptr;
   ra_status st = current_device(&d);
   if (st != RA_OK) return st;
@@ -690,6 +753,12 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
   for (const void* ptr : in)
     if (ptr == nullptr || !aligned16(ptr)) return RA_ERR_INVALID_ARG;
   if (workspace_bytes < bwd_workspace(pr)) return RA_ERR_INVALID_ARG;
+  {
+    const Bytes b = tensor_bytes(pr);
+    if (!writes_disjoint({{dq, b.q}, {dk, b.kv}, {dv, b.kv}, {workspace, bwd_workspace(pr)}},
+                         {{q, b.q}, {k, b.kv}, {v, b.kv}, {o, b.q}, {lse, b.rows}, {dout, b.q}}))
+      return RA_ERR_INVALID_ARG;
+  }
   // the extension rows are addressed by 32-bit TMA coordinates
   if (bwd_tiles(pr) * 2 * 128 + 128 >= (static_cast<int64_t>(1) << 31)) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
@@ -754,6 +823,14 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
       !aligned16(workspace))
     return RA_ERR_INVALID_ARG;
   if (workspace_bytes < decode_workspace(pr, n_q)) return RA_ERR_INVALID_ARG;
+  {
+    const Bytes b = tensor_bytes(pr);
+    const size_t qrows = static_cast<size_t>(pr->batch) * n_q * pr->heads;
+    if (!writes_disjoint({{o, qrows * pr->head_dim * 2}, {lse, qrows * sizeof(float)},
+                          {workspace, decode_workspace(pr, n_q)}},
+                         {{q, qrows * pr->head_dim * 2}, {k, b.kv}, {v, b.kv}}))
+      return RA_ERR_INVALID_ARG;
+  }
   const int64_t parts = decode_parts(pr);
   // launch limits of the partial phase (grid z = batch * P) and of the merge
   if (parts > 1024 || static_cast<int64_t>(pr->batch) * pr->P > 65535 || pr->batch > 65535 ||

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from online_softmax_merge_gb300 import _lib
 from online_softmax_merge_gb300 import build as B
@@ -202,3 +203,64 @@ def test_host_mapped_refuses_pageable_null_and_empty_ranges(lib):
     assert lib.ring_attn_host_mapped(ctypes.addressof(buf), 4096) == 0
     assert lib.ring_attn_host_mapped(None, 4096) == 0
     assert lib.ring_attn_host_mapped(ctypes.addressof(buf), 0) == 0
+
+
+# Far-apart fake addresses (aligned, never dereferenced): every range of the small
+# problems below fits between two of them.
+def _at(i, off=0):
+    return ctypes.c_void_p(0x1000_0000_0000 + i * 0x1_0000_0000 + off)
+
+
+def _no_device_reached(code):
+    """A call whose arguments passed every host-side check stops at the device lookup
+    (RA_ERR_CUDA or RA_ERR_UNSUPPORTED here); on a machine with a GPU the fake
+    addresses fail the residency check instead, so only the overlap cases are decided."""
+    if torch.cuda.is_available():
+        return True
+    return code in (_lib.RA_ERR_CUDA, _lib.RA_ERR_UNSUPPORTED)
+
+
+def test_written_ranges_may_not_overlap_other_arguments(lib):
+    pr = _pr()                                      # B=1 N=256 H=4 G=2 d=128
+    bq, bkv, brows, by = 256 * 4 * 128 * 2, 256 * 2 * 128 * 2, 4 * 256 * 4, 256 * 4 * 128 * 4
+    q, k, v, o, lse = (_at(i) for i in range(5))
+    fwd = lambda *a: lib.ring_attn_fwd(ctypes.byref(pr), *a, None)
+    assert _no_device_reached(fwd(q, k, v, o, lse))
+    assert _no_device_reached(fwd(q, k, k, o, lse))                 # inputs may alias
+    assert fwd(q, k, v, q, lse) == _lib.RA_ERR_INVALID_ARG           # o over q: no in-place form
+    assert fwd(q, k, v, _at(0, bq - 16), lse) == _lib.RA_ERR_INVALID_ARG   # o over q's tail
+    assert _no_device_reached(fwd(q, k, v, _at(0, bq), lse))        # o right after q
+    assert fwd(q, k, v, o, _at(3, bq - 16)) == _lib.RA_ERR_INVALID_ARG     # lse inside o
+    assert fwd(q, k, v, o, _at(2, bkv - 16)) == _lib.RA_ERR_INVALID_ARG    # lse over v's tail
+    m, z, y = _at(5), _at(6), _at(7)
+    step = lambda *a: lib.ring_attn_step(ctypes.byref(pr), 0, 1, *a, None)
+    assert _no_device_reached(step(q, k, v, m, z, y))
+    assert step(q, k, v, m, z, _at(1, 16)) == _lib.RA_ERR_INVALID_ARG      # y over k
+    assert step(q, k, v, m, _at(5, brows - 16), y) == _lib.RA_ERR_INVALID_ARG   # z over m
+    fin = lambda *a: lib.ring_attn_finalize(ctypes.byref(pr), *a, None)
+    assert _no_device_reached(fin(m, z, y, o, lse))
+    assert fin(m, z, y, o, _at(7, by - 16)) == _lib.RA_ERR_INVALID_ARG      # lse over y
+    n = 3
+    merge = lambda *a: lib.ring_attn_merge(n, 1, 256, 4, 128, *a, None)
+    assert _no_device_reached(merge(_at(8), _at(9), o, lse))
+    assert merge(_at(8), _at(9), _at(8, n * 256 * 4 * 128 * 4 - 16), lse) == \
+        _lib.RA_ERR_INVALID_ARG                                        # o over o_parts' tail
+    ws = _at(10)
+    need = lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr))
+    bwd = lambda *a: lib.ring_attn_bwd(ctypes.byref(pr), *a, need, None)
+    dout, dq, dk, dv = _at(11), _at(12), _at(13), _at(14)
+    assert _no_device_reached(bwd(q, k, v, o, lse, dout, dq, dk, dv, ws))
+    assert bwd(q, k, v, o, lse, dout, dout, dk, dv, ws) == _lib.RA_ERR_INVALID_ARG   # dq = dout
+    assert bwd(q, k, v, o, lse, dout, dq, dk, dv, _at(14, bkv - 16)) == \
+        _lib.RA_ERR_INVALID_ARG                                        # workspace over dv
+    assert bwd(q, k, v, o, lse, dout, dq, dk, dk, ws) == _lib.RA_ERR_INVALID_ARG     # dk = dv
+    dpr = _pr(seqlen=8192, P=4)
+    dneed = lib.ring_attn_decode_workspace_bytes(ctypes.byref(dpr), 1)
+    dec = lambda *a: lib.ring_attn_decode(ctypes.byref(dpr), 1, 8191, *a, dneed, None)
+    assert _no_device_reached(dec(q, k, v, o, lse, ws))
+    assert dec(q, k, v, o, lse, _at(1, 64)) == _lib.RA_ERR_INVALID_ARG      # workspace over k
+    hneed = lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr))
+    host = lambda *a: lib.ring_attn_fwd_host(ctypes.byref(pr), *a, hneed, None, None)
+    assert _no_device_reached(host(q, k, v, o, lse, ws))
+    assert host(q, k, v, o, lse, _at(3, 256)) == _lib.RA_ERR_INVALID_ARG    # workspace over o
+    assert host(q, k, v, o, _at(2), ws) == _lib.RA_ERR_INVALID_ARG          # lse = v

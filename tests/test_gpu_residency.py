@@ -80,3 +80,32 @@ def test_every_pytorch_allocator_is_accepted_with_identical_results():
         assert r.returncode == 0, (conf, r.stderr[-3000:])
         digests[conf] = r.stdout.strip().splitlines()[-1]
     assert len(set(digests.values())) == 1, digests
+
+
+def test_outputs_overlapping_inputs_are_refused_and_nothing_is_written():
+    """There is no in-place form: o over q, z over m, dq over dout and a
+    merge output over its partials are refused before any launch (the binding surfaces
+    RA_ERR_INVALID_ARG), and the aliased buffers keep their contents."""
+    q, k, v = (t.to(DEV) for t in make_qkv(W))
+    q0 = q.clone()
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.fwd(q, k, v, W.P, W.layout, W.causal, out=q)
+    assert e.value.code == _lib.RA_ERR_INVALID_ARG
+    o, lse = ra.fwd(q, k, k, W.P, W.layout, W.causal)              # inputs may alias
+    torch.cuda.synchronize()
+    m, z, y = ra.empty_state(q)
+    with pytest.raises(ra.RingAttnError):
+        ra.step(q, k, v, W.P, 0, (m, m, y), True, W.layout, W.causal)   # z over m
+    dout = make_dout(W).to(DEV)
+    d0 = dout.clone()
+    o, lse = ra.fwd(q, k, v, W.P, W.layout, W.causal)
+    with pytest.raises(ra.RingAttnError):
+        ra.bwd(q, k, v, o, lse, dout, W.P, W.layout, W.causal, dq=dout)
+    parts = torch.randn((3,) + tuple(o.shape), device=DEV)
+    lparts = torch.randn((3,) + tuple(lse.shape), device=DEV)
+    p0 = parts.clone()
+    with pytest.raises(ra.RingAttnError):
+        ra.merge(parts, lparts, lse=lparts[0])
+    torch.cuda.synchronize()
+    assert torch.equal(q, q0) and torch.equal(dout, d0) and torch.equal(parts, p0)
+    assert ra.last_error(DEV) == 0
