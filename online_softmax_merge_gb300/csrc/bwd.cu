@@ -98,18 +98,24 @@ struct DqSmem {
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
+// dK/dV kernel barriers. A stage's Q and dO tiles are tracked apart: dO(t) is
+// last read by dV(t), which runs before dK(t), Q's last reader, so dO(t + 2) can
+// start loading before the stage's Q slot is free.
 enum : int {
   kBarFix = 0,      // stationary tiles landed
-  kBarFull = 1,     // + stage: streamed tiles landed
-  kBarEmpty = 3,    // + stage: MMAs done with the stage
+  kBarFull = 1,     // + stage: Q tile and its extension landed
+  kBarEmpty = 3,    // + stage: dK done with the stage's Q
   kBarSF = 5,       // score tile in TMEM
   kBarDPF = 6,      // dP tile in TMEM
   kBarW1 = 7,       // workers: phase 1 done (8 arrivals)
   kBarW2 = 8,       // workers: dS written (8 arrivals)
   kBarDone = 9,     // every MMA of the CTA completed
   kBarDrain = 10,
-  kNumBars = 11
+  kBarFullO = 11,   // + stage: dO tile and its extension landed
+  kBarEmptyO = 13,  // + stage: dV done with the stage's dO
+  kNumBars = 15
 };
+static_assert(8 * kNumBars + 8 <= 256, "barrier area");
 
 __device__ __forceinline__ void record_failure(const BwdParams& p, volatile int* abort_flag) {
   atomicCAS(p.status, 0, static_cast<int>(RA_ERR_TIMEOUT));
@@ -427,7 +433,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      uint32_t nf0 = 0, nf1 = 0;   // loads issued per stage (for the drain on abort)
+      uint32_t nfq[2] = {}, nfo[2] = {};   // loads issued per barrier (for the drain on abort)
       bool ok = true;
       mbar_arrive_expect_tx(bar(kBarFix), 2 * L::kTile + kExtBytes);
 #pragma unroll
@@ -441,31 +447,45 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       walk_qtiles<ZIG>(p, w, [&](int t, int h, const Seg& sq, int qt) {
         const int st = t & 1;
         const uint32_t n = static_cast<uint32_t>(t >> 1);
+        const uint32_t dst = sbase + L::kStage + st * 2 * L::kTile;
+        const int tile = ((w.bat * p.H + h) * p.X + sq.chunk) * p.nt + qt;
+        const uint32_t ext = sbase + L::kExt + st * 2 * kExtBytes;
+        // dO(t) and its extension (-D), once dV(t - 2) has read the slot
+        if (t >= 2 && !bounded_wait(bar(kBarEmptyO + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+          ok = false;
+          return false;
+        }
+        mbar_arrive_expect_tx(bar(kBarFullO + st), L::kTile + kExtBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_rows(&tdo, dst + L::kTile + c * L::kChunk, bar(kBarFullO + st), p.layout, c, h,
+                   sq.chunk, qt * 128, w.bat);
+        tma_load_2d(ext + kExtBytes, &text, bar(kBarFullO + st), 0, (p.tiles + tile) * 128);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) nfo[x] += (x == st);
+        // Q(t) and its extension (-LSE/scale), once dK(t - 2) has read the slot
         if (t >= 2 && !bounded_wait(bar(kBarEmpty + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           return false;
         }
-        const uint32_t dst = sbase + L::kStage + st * 2 * L::kTile;
-        mbar_arrive_expect_tx(bar(kBarFull + st), 2 * L::kTile + 2 * kExtBytes);
+        mbar_arrive_expect_tx(bar(kBarFull + st), L::kTile + kExtBytes);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 64; ++c)
           tma_rows(&tq, dst + c * L::kChunk, bar(kBarFull + st), p.layout, c, h, sq.chunk,
                    qt * 128, w.bat);
-          tma_rows(&tdo, dst + L::kTile + c * L::kChunk, bar(kBarFull + st), p.layout, c, h,
-                   sq.chunk, qt * 128, w.bat);
-        }
-        const int tile = ((w.bat * p.H + h) * p.X + sq.chunk) * p.nt + qt;
-        const uint32_t ext = sbase + L::kExt + st * 2 * kExtBytes;
         tma_load_2d(ext, &text, bar(kBarFull + st), 0, tile * 128);
-        tma_load_2d(ext + kExtBytes, &text, bar(kBarFull + st), 0, (p.tiles + tile) * 128);
-        if (st) ++nf1; else ++nf0;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) nfq[x] += (x == st);
         return true;
       });
       if (!ok) {
         record_failure(p, abort_flag);
         bounded_wait(bar(kBarFix), 0, kDrainNs, nullptr);
-        if (nf0) bounded_wait(bar(kBarFull), (nf0 - 1) & 1, kDrainNs, nullptr);
-        if (nf1) bounded_wait(bar(kBarFull + 1), (nf1 - 1) & 1, kDrainNs, nullptr);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (nfq[x]) bounded_wait(bar(kBarFull + x), (nfq[x] - 1) & 1, kDrainNs, nullptr);
+          if (nfo[x]) bounded_wait(bar(kBarFullO + x), (nfo[x] - 1) & 1, kDrainNs, nullptr);
+        }
       }
     }
     __syncwarp();
@@ -496,6 +516,13 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       if (elect_one()) {
         products(0, 0);     // S^T(0) = K Q^T - LSE/scale
         mma_commit(bar(kBarSF));
+      }
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, bounded_wait(bar(kBarFullO), 0, p.timeout_ns, abort_flag));
+    }
+    if (ok) {
+      tc_fence_after_sync();
+      if (elect_one()) {
         products(0, 1);     // dP^T(0) = V dO^T - D
         mma_commit(bar(kBarDPF));
       }
@@ -511,7 +538,10 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         break;
       }
       tc_fence_after_sync();
-      if (elect_one()) issue_ts<D>(tDV, tS, sdesc(st, 1, true), t > 0);   // dV += A^T dO
+      if (elect_one()) {
+        issue_ts<D>(tDV, tS, sdesc(st, 1, true), t > 0);   // dV += A^T dO
+        mma_commit(bar(kBarEmptyO + st));
+      }
       __syncwarp();
       if (has_next) {
         if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarFull + st1), ph1, p.timeout_ns, abort_flag))) {
@@ -533,14 +563,21 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       if (elect_one()) {
         issue_ts<D>(tDK, tDP, sdesc(st, 0, true), t > 0);          // dK += dS^T Q
         mma_commit(bar(kBarEmpty + st));
-        if (has_next) {
-          products(st1, 1);
-          mma_commit(bar(kBarDPF));
-        } else {
-          mma_commit(bar(kBarDone));
-        }
+        if (!has_next) mma_commit(bar(kBarDone));
       }
       __syncwarp();
+      if (has_next) {
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarFullO + st1), ph1, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (elect_one()) {
+          products(st1, 1);
+          mma_commit(bar(kBarDPF));
+        }
+        __syncwarp();
+      }
     }
     if (!ok) {
       if (lane == 0) record_failure(p, abort_flag);
