@@ -43,7 +43,9 @@
 // first three columns, the query side the bf16 split hi + mid + lo of -LSE/scale
 // (for S^T) or of -D (for dP^T), so the tensor core returns S^T - LSE/scale and
 // dP^T - D in fp32 (three bf16 terms carry ~24 significant bits) and the workers
-// need no per-column statistics.
+// need no per-column statistics. A stage's Q and dO have their own full and
+// empty barriers: dO(t) is last read by dV(t), which completes before dK(t)
+// reads Q(t) for the last time, so dO(t + 2) is loaded without waiting for dK(t).
 // dQ kernel, per key tile t (TMEM: S [0,128), dP [128,256), dQ [256,256+D),
 // Q and dO as bf16 pairs [384,512)): MMA order  dP(t) | S(t+1) | dQ += dS(t) K(t)
 // | dP(t+1) ...
