@@ -335,10 +335,12 @@ def run_reference(args, w):
 L2_FLUSH_BELOW = 1 << 30     # bytes of Q, K, V, O and LSE under which the L2 is flushed
 
 
-def workload_bytes(w) -> int:
-    """Bytes of the forward's inputs and outputs (Q, K, V, O in bf16, LSE in fp32)."""
+def workload_bytes(w, o_bytes: int = 2) -> int:
+    """Bytes of the forward's inputs and outputs (Q, K, V in bf16, O in bf16 or fp32,
+    LSE in fp32)."""
     tok = w.batch * w.seqlen
-    return tok * (2 * w.heads + 2 * w.kv_heads) * w.head_dim * 2 + tok * w.heads * 4
+    return (tok * (w.heads + 2 * w.kv_heads) * w.head_dim * 2 +
+            tok * w.heads * w.head_dim * o_bytes + tok * w.heads * 4)
 
 
 def config_obj(w, args):
@@ -349,12 +351,20 @@ def config_obj(w, args):
     return {"workload": f"{w.name}: {text}", "batch": w.batch,
             "seqlen": w.seqlen, "heads": w.heads, "kv_heads": w.kv_heads,
             "head_dim": w.head_dim, "P": w.P, "layout": w.layout, "causal": w.causal,
-            "seed": w.seed,
+            "seed": w.seed, "out_dtype": args.out_dtype,
             "l2": ("L2 flushed (256 MB write) before every timed step; time = sum of the "
                    "per-step CUDA events" if workload_bytes(w) < L2_FLUSH_BELOW else
-                   f"inputs and outputs {workload_bytes(w) / 1e9:.1f} GB, larger than the "
-                   "129 MB L2 (no flush needed)"),
+                   f"inputs and outputs {workload_bytes(w, o_bytes(args)) / 1e9:.1f} GB, larger "
+                   "than the 129 MB L2 (no flush needed)"),
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def out_dtype(args):
+    return torch.float32 if args.out_dtype == "fp32" else torch.bfloat16
+
+
+def o_bytes(args) -> int:
+    return 4 if args.out_dtype == "fp32" else 2
 
 
 def time_launches(fn, steps, stream):
@@ -380,12 +390,13 @@ def run_ours(args, w):
     ra.load()
 
     q, k, v = make_qkv(w, device=dev)
-    o = torch.empty((w.batch, w.seqlen, w.heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+    odt = out_dtype(args)
+    o = torch.empty((w.batch, w.seqlen, w.heads, w.head_dim), dtype=odt, device=dev)
     lse = torch.empty((w.batch, w.heads, w.seqlen), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        ra.fwd(q, k, v, w.P, w.layout, w.causal, out=o, lse=lse)
+        ra.fwd(q, k, v, w.P, w.layout, w.causal, out=o, lse=lse, out_dtype=odt)
 
     for _ in range(args.warmup):
         step()
@@ -396,7 +407,7 @@ def run_ours(args, w):
     # ---- timed region: K steps, inputs resident in HBM. A workload whose tensors are
     # not far above the 129 MB L2 gets the L2 flushed (a 256 MB write) before every
     # step, and its time is the sum of the per-step events, which exclude the flushes.
-    flush = workload_bytes(w) < L2_FLUSH_BELOW
+    flush = workload_bytes(w, o_bytes(args)) < L2_FLUSH_BELOW
     scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
     replicas.barrier(info)
     torch.cuda.synchronize(dev)
@@ -437,6 +448,28 @@ def run_ours(args, w):
     achieved = flops_step / mean_launch_s / 1e12
     traffic = load_traffic(f"ring_tc_kernel:{w.name}")
 
+    # ---- the same forward writing O in the other element type (bf16 <-> fp32)
+    other = None
+    if not args.no_other_out:
+        odt2 = torch.bfloat16 if odt == torch.float32 else torch.float32
+        o2 = torch.empty(o.shape, dtype=odt2, device=dev)
+        l2 = torch.empty_like(lse)
+
+        def other_step():
+            ra.fwd(q, k, v, w.P, w.layout, w.causal, out=o2, lse=l2, out_dtype=odt2)
+
+        other_step()
+        ms = time_launches(other_step, max(2, min(args.steps, 3)), stream)
+        # one computation, two stores: the bf16 output is the fp32 one rounded
+        o32, o16 = (o, o2) if odt == torch.float32 else (o2, o)
+        other = {"out_dtype": "fp32" if odt2 == torch.float32 else "bf16",
+                 "ms": statistics.mean(ms),
+                 "achieved": flops_step / (statistics.mean(ms) * 1e-3) / 1e12,
+                 "unit": "TFLOP/s",
+                 "bf16_is_rounded_fp32": bool(torch.equal(o16, o32.to(torch.bfloat16))),
+                 "lse_equal": bool(torch.equal(l2, lse))}
+        del o2, l2, o32, o16
+
     # ---- e2e through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -447,14 +480,15 @@ def run_ours(args, w):
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         hws = torch.empty(ra.fwd_host_workspace_bytes(w.batch, w.seqlen, w.heads, w.kv_heads,
-                                                      w.head_dim, w.P, w.layout, w.causal),
+                                                      w.head_dim, w.P, w.layout, w.causal,
+                                                      out_dtype=odt),
                           dtype=torch.uint8, device=dev)
 
         def e2e_step():
             # the public call for host-resident inputs: copies in, the ring forward
             # and copies out, pipelined one sequence at a time
             ra.fwd_host(hq, hk, hv, w.P, w.layout, w.causal, out=ho, lse=hl, workspace=hws,
-                        device=dev)
+                        device=dev, out_dtype=odt)
 
         e2e_step()
         torch.cuda.synchronize(dev)
@@ -468,7 +502,7 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         e_ms = replicas.max_over_ranks(info, a.elapsed_time(b), device=dev)
         h2d = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
-        d2h = o.numel() * 2 + lse.numel() * 4
+        d2h = o.numel() * o.element_size() + lse.numel() * 4
         e2e = {"value": info.world * flops_step * e2e_steps / (e_ms * 1e-3) / 1e12,
                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e2e_steps, "ms_per_step": e_ms / e2e_steps}
@@ -534,7 +568,7 @@ def run_ours(args, w):
         def composed():
             for s in range(w.P):
                 ra.step(q, k, v, w.P, s, state, s == 0, w.layout, w.causal)
-            ra.finalize(state, w.P, w.layout, w.causal, out=so, lse=sl)
+            ra.finalize(state, w.P, w.layout, w.causal, out=so, lse=sl, out_dtype=odt)
 
         composed()
         torch.cuda.synchronize(dev)
@@ -607,6 +641,7 @@ def run_ours(args, w):
             "data": "synthetic", "config": config_obj(w, args),
             "tokens_per_s": tokens_s, "pct_bf16_peak": 100.0 * value / (info.world * peak_tf),
             "flops_per_step": flops_step,
+            "fwd_other_out": other,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic,
                          "peak_source": f"{peaks_src} bf16 burst",
@@ -640,6 +675,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     ap.add_argument("--one-core-seconds", type=float, default=6.0)
+    ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "fp32"],
+                    help="element type of O written by the timed forward (and e2e)")
+    ap.add_argument("--no-other-out", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-merge", action="store_true")
     ap.add_argument("--no-decode", action="store_true")

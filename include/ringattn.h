@@ -20,7 +20,8 @@
  * ---------------------------------------
  *  Tensors are in ORIGINAL token order whatever the shard layout (the layout is
  *  an index map, not a permutation of memory):
- *    q, o        [B, N, H, d]  bf16, row-major (d fastest)
+ *    q           [B, N, H, d]  bf16, row-major (d fastest)
+ *    o           [B, N, H, d]  bf16, or fp32 when p->o_dtype == RA_DTYPE_F32
  *    k, v        [B, N, G, d]  bf16
  *    lse, m, z   [B, H, N]     fp32
  *    y           [B, N, H, d]  fp32
@@ -45,8 +46,10 @@
  *  concurrent calls on different streams are safe when their output buffers
  *  (and workspaces) do not overlap.
  *
- *  CUDA graphs: after a device's first eager call of an entry point (which sets
- *  the kernels' shared-memory limits and reads the device's facts), the calls
+ *  CUDA graphs: after the first eager call of an entry point in a device's
+ *  context (which sets the kernels' shared-memory limits and reads the device's
+ *  facts; a context made anew, e.g. after cudaDeviceReset, gets the same first
+ *  step at its first call, since the library keys these facts by context), the calls
  *  that launch kernels on `stream` only — every one but ring_attn_fwd_host and
  *  ring_attn_last_error — may be captured into a graph; a replay computes what
  *  the eager call would on the buffers' contents at replay time.
@@ -100,6 +103,14 @@ typedef enum {
                                then chunk 2P-1-u (local C..2C-1); needs N % (2P) == 0 */
 } ra_layout;
 
+/* Element type of the output O (ra_problem.o_dtype). bf16 is the usual attention
+ * output. fp32 keeps the fp32 result of the division O = y / z. Rounding O to bf16
+ * adds up to half a bf16 unit in the last place: 0.0078 for 2 <= |O| < 4 and
+ * 0.0156 for 4 <= |O| < 8, so an absolute error bound of 1e-2 at every magnitude
+ * holds only for the fp32 output. Both are results of the same computation (bf16
+ * inputs, fp32 accumulation). */
+typedef enum { RA_DTYPE_BF16 = 0, RA_DTYPE_F32 = 1 } ra_dtype;
+
 /* Tile classes of a (query tile, key tile) pair ("Part 4" §4.8.1 "Skipping
  * Fully-Masked Blocks"). */
 typedef enum { RA_TILE_EMPTY = 0, RA_TILE_PARTIAL = 1, RA_TILE_FULL = 2 } ra_tile_class;
@@ -118,6 +129,10 @@ typedef struct {
   int32_t causal;     /* 0 or 1 */
   int32_t layout;     /* ra_layout */
   float scale;        /* score scale; 0 means 1/sqrt(d) */
+  int32_t o_dtype;    /* ra_dtype of o (0 = bf16, the default of a zeroed struct); read by
+                         ring_attn_fwd, ring_attn_fwd_host, ring_attn_finalize,
+                         ring_attn_decode(_noalloc) (written o) and ring_attn_bwd (the saved
+                         o it reads); the step calls ignore it */
 } ra_problem;
 
 /* Full ring forward: every virtual device u folds all P shards in ring order
@@ -251,16 +266,21 @@ size_t ring_attn_decode_workspace_bytes(const ra_problem* p, int32_t n_q);
  * serving loop that must not stall on an allocator, a plugin whose host owns all
  * device memory, a runtime that plans memory up front). Same contract and result
  * as ring_attn_decode, but the partials go to a fixed scratch array of
- * RA_DECODE_SCRATCH_BYTES bytes in the library's static device memory (reserved
- * on every GPU that loads the library, until the process exits) instead of a
- * caller workspace; the call allocates nothing. There is no counterpart in the
- * pages: this is an interface choice of this library.
+ * RA_DECODE_SCRATCH_BYTES bytes in the library's static device memory instead of
+ * a caller workspace. There is no counterpart in the pages: this is an interface
+ * choice of this library.
  * Returns RA_ERR_INVALID_ARG when ring_attn_decode_workspace_bytes(p, n_q) exceeds
- * RA_DECODE_SCRATCH_BYTES. The first call on a device looks up the scratch
- * address (cudaGetSymbolAddress) with that device current; make that first call
- * before capturing a stream. All calls on a device share the scratch and each
- * call overwrites it: calls whose work may overlap on the GPU (different streams
- * without ordering) race. */
+ * RA_DECODE_SCRATCH_BYTES.
+ * First call on a device: the CUDA runtime loads modules lazily, so the first call
+ * on a device (more exactly: in a device context) loads the module that holds the
+ * array, which reserves its RA_DECODE_SCRATCH_BYTES on that device until the
+ * process exits, and looks up its address (cudaGetSymbolAddress) with the device
+ * current. That call can return RA_ERR_CUDA if the device has no room for the
+ * array (no CUDA error is left pending); make it before capturing a stream. Later
+ * calls in the same context allocate nothing; a new context (after
+ * cudaDeviceReset) repeats the first-call step.
+ * All calls on a device share the scratch and each call overwrites it: calls
+ * whose work may overlap on the GPU (different streams without ordering) race. */
 ra_status ring_attn_decode_noalloc(const ra_problem* p, int32_t n_q, int32_t q_pos0,
                                    const void* q, const void* k, const void* v, void* o,
                                    float* lse, void* stream);
@@ -329,6 +349,17 @@ ra_status ring_attn_last_error(int32_t* device_code);
  * records RA_ERR_TIMEOUT in the status word and returns. Lets a test see the
  * timeout path without a hang. 0 < limit_ns <= 10^9. */
 ra_status ring_attn_selftest_timeout(uint64_t limit_ns, void* stream);
+
+/* Test hook for the kernels' abort path. Sets the time limit of every device-side
+ * wait of the forward, step, backward and decode kernels launched by later calls
+ * in this process (all devices) to limit_ns nanoseconds; 0 restores the default,
+ * 2 s. A limit of a few nanoseconds makes real waits of those kernels run out on
+ * an ordinary problem: the kernel that gives up records RA_ERR_TIMEOUT, stops its
+ * other roles through a shared flag, lets the copies and products it has in flight
+ * finish (those waits keep their own fixed limit), frees its tensor memory and
+ * returns, and its outputs are undefined. Meant for tests only: an application has
+ * no reason to call it. Limits above the default give RA_ERR_INVALID_ARG. */
+ra_status ring_attn_selftest_wait_limit(uint64_t limit_ns);
 
 /* 1 if this library was built with the kernels' index checks (RA_DEBUG), else 0.
  * In such a debug build every raw global load or store (one that is not a TMA copy)

@@ -6,7 +6,9 @@ and pass raw pointers plus the current CUDA stream. Every step of the path runs
 in the library's CUDA kernels; nothing here computes attention.
 
 Tensor layouts (original token order, whatever the shard layout):
-  q, o [B, N, H, d] bf16;  k, v [B, N, G, d] bf16;  lse, m, z [B, H, N] fp32;
+  q [B, N, H, d] bf16;  o [B, N, H, d] bf16, or fp32 where a call takes
+  out_dtype=torch.float32 (O kept at fp32, not rounded to bf16);
+  k, v [B, N, G, d] bf16;  lse, m, z [B, H, N] fp32;
   y [B, N, H, d] fp32;  o_parts [n, B, N, H, d] fp32;  lse_parts [n, B, H, N] fp32.
 """
 from __future__ import annotations
@@ -22,6 +24,7 @@ from ._lib import (LAYOUTS, RA_ERR_BOUNDS, RA_ERR_CUDA, RA_ERR_INVALID_ARG,  # n
 
 __all__ = ["fwd", "fwd_host", "fwd_host_workspace_bytes", "host_mapped", "bwd", "bwd_workspace_bytes", "decode", "decode_workspace_bytes", "step", "step_simt", "finalize", "merge", "shard_map", "shard_map_device",
            "tile_classes", "mask", "last_error", "selftest_timeout", "selftest_bounds",
+           "selftest_wait_limit",
            "debug_checks", "problem", "RingAttnError",
            "empty_state", "LAYOUTS", "TILE"]
 
@@ -54,16 +57,27 @@ def _same_device(ref: torch.Tensor, **tensors):
             raise ValueError(f"{name} is on {t.device}, the call runs on {ref.device}")
 
 
+_O_DTYPES = {torch.bfloat16: _lib.RA_DTYPE_BF16, torch.float32: _lib.RA_DTYPE_F32}
+
+
+def _o_dtype_code(out_dtype) -> int:
+    if out_dtype not in _O_DTYPES:
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
+    return _O_DTYPES[out_dtype]
+
+
 def problem(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int, P: int,
-            causal: bool, layout: str = "contiguous", scale: float = 0.0) -> _lib.RaProblem:
-    """The ra_problem struct (scale 0 means 1/sqrt(head_dim))."""
+            causal: bool, layout: str = "contiguous", scale: float = 0.0,
+            out_dtype=torch.bfloat16) -> _lib.RaProblem:
+    """The ra_problem struct (scale 0 means 1/sqrt(head_dim); out_dtype is the
+    element type of o)."""
     if layout not in LAYOUTS:
         raise ValueError(f"layout must be one of {tuple(LAYOUTS)}")
     return _lib.RaProblem(batch, seqlen, heads, kv_heads, head_dim, P, int(bool(causal)),
-                          LAYOUTS[layout], float(scale))
+                          LAYOUTS[layout], float(scale), _o_dtype_code(out_dtype))
 
 
-def _qkv_problem(q, k, v, P, layout, causal, scale):
+def _qkv_problem(q, k, v, P, layout, causal, scale, out_dtype=torch.bfloat16):
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q must be [B, N, H, d] and k, v [B, N, G, d]")
     B, N, H, d = q.shape
@@ -73,20 +87,22 @@ def _qkv_problem(q, k, v, P, layout, causal, scale):
     _need(v, "v", torch.bfloat16, (B, N, G, d))
     if k.device != q.device or v.device != q.device:
         raise ValueError("q, k, v must be on one device")
-    return problem(B, N, H, G, d, P, causal, layout, scale), (B, N, H, G, d)
+    return problem(B, N, H, G, d, P, causal, layout, scale, out_dtype), (B, N, H, G, d)
 
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str = "contiguous",
         causal: bool = True, scale: float = 0.0, out: Optional[torch.Tensor] = None,
-        lse: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Full ring forward over P virtual shards (ring_attn_fwd). Returns (O, LSE)."""
+        lse: Optional[torch.Tensor] = None,
+        out_dtype=torch.bfloat16) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Full ring forward over P virtual shards (ring_attn_fwd). Returns (O, LSE);
+    O is bf16, or fp32 with out_dtype=torch.float32."""
     lib = load()
-    pr, (B, N, H, G, d) = _qkv_problem(q, k, v, P, layout, causal, scale)
+    pr, (B, N, H, G, d) = _qkv_problem(q, k, v, P, layout, causal, scale, out_dtype)
     if out is None:
-        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, N, H, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _need(out, "out", torch.bfloat16, (B, N, H, d))
+    _need(out, "out", out_dtype, (B, N, H, d))
     _need(lse, "lse", torch.float32, (B, H, N))
     _same_device(q, out=out, lse=lse)
     with torch.cuda.device(q.device):
@@ -112,10 +128,11 @@ _COPY_STREAMS = {}
 
 
 def fwd_host_workspace_bytes(batch: int, seqlen: int, heads: int, kv_heads: int, head_dim: int,
-                             P: int, layout: str = "contiguous", causal: bool = True) -> int:
+                             P: int, layout: str = "contiguous", causal: bool = True,
+                             out_dtype=torch.bfloat16) -> int:
     """Device workspace bytes ring_attn_fwd_host needs."""
     lib = load()
-    pr = problem(batch, seqlen, heads, kv_heads, head_dim, P, causal, layout)
+    pr = problem(batch, seqlen, heads, kv_heads, head_dim, P, causal, layout, 0.0, out_dtype)
     return int(lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr)))
 
 
@@ -123,9 +140,10 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
              layout: str = "contiguous", causal: bool = True, scale: float = 0.0,
              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, device=None,
-             copy_stream: Optional[torch.cuda.Stream] = None):
+             copy_stream: Optional[torch.cuda.Stream] = None, out_dtype=torch.bfloat16):
     """Ring forward for host tensors (ring_attn_fwd_host): q [B, N, H, d], k, v
-    [B, N, G, d] bf16 on the CPU (pinned for overlap); returns host (O, LSE). Runs
+    [B, N, G, d] bf16 on the CPU (pinned for overlap); returns host (O, LSE), O in
+    out_dtype (bf16 or fp32). Runs
     on `device` (default: the current CUDA device) and its current stream; copies
     go on copy_stream (default: one cached side stream per device)."""
     lib = load()
@@ -137,7 +155,7 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
     _need_host(k, "k", torch.bfloat16, (B, N, G, d))
     _need_host(v, "v", torch.bfloat16, (B, N, G, d))
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    pr = problem(B, N, H, G, d, P, causal, layout, scale)
+    pr = problem(B, N, H, G, d, P, causal, layout, scale, out_dtype)
     need = int(lib.ring_attn_fwd_host_workspace_bytes(ctypes.byref(pr)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
@@ -149,10 +167,10 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int,
         raise ValueError(f"workspace is on {workspace.device}, the call runs on {dev}")
     pin = q.is_pinned()
     if out is None:
-        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, pin_memory=pin)
+        out = torch.empty((B, N, H, d), dtype=out_dtype, pin_memory=pin)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
-    _need_host(out, "out", torch.bfloat16, (B, N, H, d))
+    _need_host(out, "out", out_dtype, (B, N, H, d))
     _need_host(lse, "lse", torch.float32, (B, H, N))
     if copy_stream is None:
         copy_stream = _COPY_STREAMS.get(dev.index)
@@ -193,10 +211,11 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
         scale: float = 0.0, dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
         dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
     """Backward ring (ring_attn_bwd): gradients of the forward for upstream gradient
-    dout, from the forward's saved o and lse. Returns (dq, dk, dv)."""
+    dout, from the forward's saved o (bf16 or fp32) and lse. Returns (dq, dk, dv)."""
     lib = load()
-    pr, (B, N, H, G, d) = _qkv_problem(q, k, v, P, layout, causal, scale)
-    _need(o, "o", torch.bfloat16, (B, N, H, d))
+    pr, (B, N, H, G, d) = _qkv_problem(q, k, v, P, layout, causal, scale,
+                                       o.dtype if o.dtype == torch.float32 else torch.bfloat16)
+    _need(o, "o", torch.bfloat16 if o.dtype != torch.float32 else torch.float32, (B, N, H, d))
     _need(lse, "lse", torch.float32, (B, H, N))
     _need(dout, "dout", torch.bfloat16, (B, N, H, d))
     need = int(lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr)))
@@ -232,9 +251,10 @@ def decode_workspace_bytes(batch: int, seqlen: int, heads: int, kv_heads: int, h
 def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, q_pos0: int,
            layout: str = "contiguous", causal: bool = True, scale: float = 0.0,
            workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-           lse: Optional[torch.Tensor] = None):
+           lse: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16):
     """Pass-Q decode (ring_attn_decode): q [B, n_q, H, d] at positions q_pos0.. against the
-    KV cache k, v [B, N, G, d] in P stationary virtual shards. Returns (O, LSE)."""
+    KV cache k, v [B, N, G, d] in P stationary virtual shards. Returns (O, LSE), O in
+    out_dtype (bf16 or fp32)."""
     lib = load()
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("q must be [B, n_q, H, d] and k, v [B, N, G, d]")
@@ -243,16 +263,16 @@ def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, q_pos0: in
     _need(q, "q", torch.bfloat16)
     _need(k, "k", torch.bfloat16, (B, N, G, d))
     _need(v, "v", torch.bfloat16, (B, N, G, d))
-    pr = problem(B, N, H, G, d, P, causal, layout, scale)
+    pr = problem(B, N, H, G, d, P, causal, layout, scale, out_dtype)
     need = int(lib.ring_attn_decode_workspace_bytes(ctypes.byref(pr), n_q))
     if workspace is None:
         workspace = torch.empty(max(need, 16) // 4 + 4, dtype=torch.float32, device=q.device)
     _need(workspace, "workspace", torch.float32)
     if out is None:
-        out = torch.empty((B, n_q, H, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, n_q, H, d), dtype=out_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
-    _need(out, "out", torch.bfloat16, (B, n_q, H, d))
+    _need(out, "out", out_dtype, (B, n_q, H, d))
     _need(lse, "lse", torch.float32, (B, H, n_q))
     _same_device(q, k=k, v=v, workspace=workspace, out=out, lse=lse)
     with torch.cuda.device(q.device):
@@ -300,8 +320,9 @@ def step_simt(q, k, v, P: int, s: int, state, first: bool, layout: str = "contig
 
 
 def finalize(state, P: int = 1, layout: str = "contiguous", causal: bool = True,
-             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
-    """(m, z, y) -> (O, LSE) (ring_attn_finalize)."""
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             out_dtype=torch.bfloat16):
+    """(m, z, y) -> (O, LSE) (ring_attn_finalize); O in out_dtype (bf16 or fp32)."""
     lib = load()
     m, z, y = state
     B, N, H, d = y.shape
@@ -309,13 +330,13 @@ def finalize(state, P: int = 1, layout: str = "contiguous", causal: bool = True,
     _need(m, "m", torch.float32, (B, H, N))
     _need(z, "z", torch.float32, (B, H, N))
     if out is None:
-        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=y.device)
+        out = torch.empty((B, N, H, d), dtype=out_dtype, device=y.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=y.device)
-    _need(out, "out", torch.bfloat16, (B, N, H, d))
+    _need(out, "out", out_dtype, (B, N, H, d))
     _need(lse, "lse", torch.float32, (B, H, N))
     _same_device(y, m=m, z=z, out=out, lse=lse)
-    pr = problem(B, N, H, H, d, P, causal, layout)
+    pr = problem(B, N, H, H, d, P, causal, layout, 0.0, out_dtype)
     with torch.cuda.device(y.device):
         check("ring_attn_finalize", lib.ring_attn_finalize(ctypes.byref(pr), _ptr(m), _ptr(z),
                                                            _ptr(y), _ptr(out), _ptr(lse),
@@ -425,3 +446,10 @@ def selftest_timeout(limit_ns: int, device="cuda") -> None:
     with torch.cuda.device(device):
         check("ring_attn_selftest_timeout",
               lib.ring_attn_selftest_timeout(int(limit_ns), _stream(device)))
+
+
+def selftest_wait_limit(limit_ns: int) -> None:
+    """Test hook (ring_attn_selftest_wait_limit): the time limit of every device-side
+    wait in the kernels of later calls; 0 restores the default (2 s). A few
+    nanoseconds make the kernels' real waits run out, exercising their abort path."""
+    check("ring_attn_selftest_wait_limit", load().ring_attn_selftest_wait_limit(int(limit_ns)))

@@ -17,7 +17,10 @@ RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_E
 STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
                 4: "RA_ERR_TIMEOUT", 5: "RA_ERR_BOUNDS"}
 LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
+RA_DTYPE_BF16, RA_DTYPE_F32 = 0, 1
 TILE = 128
+# bytes of the fixed scratch array of ring_attn_decode_noalloc (RA_DECODE_SCRATCH_BYTES)
+RA_DECODE_SCRATCH_BYTES = 16 << 20
 
 # Every exported function of include/ringattn.h, with (restype, argtypes).
 _i32, _u64, _vp, _fp = ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p
@@ -26,7 +29,8 @@ _i32, _u64, _vp, _fp = ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p, ctypes.
 class RaProblem(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32), ("heads", ctypes.c_int32),
                 ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("P", ctypes.c_int32),
-                ("causal", ctypes.c_int32), ("layout", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("causal", ctypes.c_int32), ("layout", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("o_dtype", ctypes.c_int32)]
 
 
 _PP = ctypes.POINTER(RaProblem)
@@ -50,6 +54,7 @@ SIGNATURES = {
     "ring_attn_mask": (_i32, [_PP, _i32, _i32, _vp, _vp]),
     "ring_attn_last_error": (_i32, [ctypes.POINTER(ctypes.c_int32)]),
     "ring_attn_selftest_timeout": (_i32, [_u64, _vp]),
+    "ring_attn_selftest_wait_limit": (_i32, [_u64]),
     "ring_attn_selftest_bounds": (_i32, [_vp]),
     "ring_attn_debug_checks": (_i32, []),
     "ra_status_str": (ctypes.c_char_p, [_i32]),

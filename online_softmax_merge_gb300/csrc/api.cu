@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <initializer_list>
 #include <mutex>
 #include <new>
@@ -13,42 +14,88 @@
 
 using namespace ra;
 
+namespace ra {
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+            cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+            cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+      get_id = reinterpret_cast<CtxGetIdFn>(b);
+    }
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+}  // namespace ra
+
 namespace {
 
 // Status word of the GPU: a kernel that gives up on a wait records its code here.
 __device__ int g_status = 0;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single device-side wait
+// The limit later launches get: kWaitLimitNs unless a test lowered it
+// (ring_attn_selftest_wait_limit).
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 constexpr int kMaxDevices = 64;
 
 struct DevInfo {
   bool init = false;
   bool sm103 = false;
   int ordinal = -1;
+  unsigned long long ctx = 0;   // context the facts below were read in (0: unknown)
   int* status = nullptr;
 };
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 
 // Current device's facts; RA_ERR_UNSUPPORTED unless it is compute capability 10.3.
+// They are read again whenever the current context is not the one they were read in
+// (the status word's device address belongs to a context).
 ra_status current_device(DevInfo** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lk(g_mu);
   DevInfo& d = g_dev[dev];
-  if (!d.init) {
+  if (!d.init || id == 0 || d.ctx != id) {
+    d.init = false;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return RA_ERR_CUDA;
     d.sm103 = (major == 10 && minor == 3);
     d.ordinal = dev;
+    d.status = nullptr;
     if (d.sm103) {
       void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return RA_ERR_CUDA;
+      if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return RA_ERR_CUDA;
+      }
       d.status = static_cast<int*>(ptr);
     }
+    d.ctx = current_context_id();   // the lookup made the device's context current
     d.init = true;
   }
   *out = &d;
@@ -85,7 +132,7 @@ bool writes_disjoint(std::initializer_list<Span> writes, std::initializer_list<S
 // Bytes of the tensors of a problem: q and o, k and v, one [B, H, N] fp32 row set
 // (lse, m, z), and y.
 struct Bytes {
-  size_t q, kv, rows, y;
+  size_t q, kv, rows, y, o;
 };
 Bytes tensor_bytes(const ra_problem* pr) {
   const size_t tok = static_cast<size_t>(pr->batch) * static_cast<size_t>(pr->seqlen);
@@ -94,6 +141,7 @@ Bytes tensor_bytes(const ra_problem* pr) {
   b.kv = tok * pr->kv_heads * pr->head_dim * 2;
   b.rows = tok * pr->heads * sizeof(float);
   b.y = tok * pr->heads * pr->head_dim * sizeof(float);
+  b.o = pr->o_dtype == RA_DTYPE_F32 ? b.y : b.q;
   return b;
 }
 
@@ -137,6 +185,7 @@ ra_status check_problem(const ra_problem* pr) {
     return RA_ERR_INVALID_ARG;
   if (pr->layout == RA_LAYOUT_ZIGZAG && pr->seqlen % (2 * pr->P) != 0) return RA_ERR_INVALID_ARG;
   if (!(pr->scale >= 0.f) || isinf(pr->scale)) return RA_ERR_INVALID_ARG;
+  if (pr->o_dtype != RA_DTYPE_BF16 && pr->o_dtype != RA_DTYPE_F32) return RA_ERR_INVALID_ARG;
   if (pr->head_dim != 64 && pr->head_dim != 128) return RA_ERR_UNSUPPORTED;
   // every tensor's element count must fit the kernels' 64-bit offsets and the
   // tensor-map extents (< 2^32 per dimension)
@@ -163,6 +212,7 @@ void fill_params(const ra_problem* pr, RingParams* p) {
   p->S = pr->seqlen / pr->P;
   p->layout = pr->layout;
   p->causal = pr->causal;
+  p->o_f32 = pr->o_dtype == RA_DTYPE_F32 ? 1 : 0;
   const int hpg = p->H / p->G;
   p->pair_heads = (hpg % 2 == 0) ? 1 : 0;
   p->X = p->layout == kZigzag ? 2 * p->P : p->P;
@@ -179,7 +229,7 @@ void fill_params(const ra_problem* pr, RingParams* p) {
   const double sc = pr->scale > 0.f ? static_cast<double>(pr->scale) : 1.0 / sqrt(static_cast<double>(p->D));
   p->scale = static_cast<float>(sc);
   p->scale_log2 = static_cast<float>(sc * 1.4426950408889634);
-  p->timeout_ns = kWaitLimitNs;
+  p->timeout_ns = g_wait_limit_ns.load();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -320,7 +370,8 @@ HostSlot host_slot(const ra_problem* pr) {
   HostSlot s;
   s.q = r256(static_cast<size_t>(pr->seqlen) * hpg * pr->head_dim * 2);
   s.kv = r256(static_cast<size_t>(pr->seqlen) * pr->head_dim * 2);
-  s.o = s.q;
+  s.o = r256(static_cast<size_t>(pr->seqlen) * hpg * pr->head_dim *
+             (pr->o_dtype == RA_DTYPE_F32 ? 4 : 2));
   s.lse = r256(hpg * pr->seqlen * sizeof(float));
   s.total = s.q + 2 * s.kv + s.o + s.lse;
   return s;
@@ -399,7 +450,7 @@ ra_status ring_attn_fwd(const ra_problem* pr, const void* q, const void* k, cons
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return RA_ERR_INVALID_ARG;
   const Bytes b = tensor_bytes(pr);
-  if (!writes_disjoint({{o, b.q}, {lse, b.rows}}, {{q, b.q}, {k, b.kv}, {v, b.kv}}))
+  if (!writes_disjoint({{o, b.o}, {lse, b.rows}}, {{q, b.q}, {k, b.kv}, {v, b.kv}}))
     return RA_ERR_INVALID_ARG;
   DevInfo* d = nullptr;
   if ((st = current_device(&d)) != RA_OK) return st;
@@ -432,7 +483,7 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   if (workspace_bytes < fwd_host_min_workspace(pr)) return RA_ERR_INVALID_ARG;
   {
     const Bytes b = tensor_bytes(pr);
-    if (!writes_disjoint({{o, b.q}, {lse, b.rows}, {workspace, workspace_bytes}},
+    if (!writes_disjoint({{o, b.o}, {lse, b.rows}, {workspace, workspace_bytes}},
                          {{q, b.q}, {k, b.kv}, {v, b.kv}}))
       return RA_ERR_INVALID_ARG;
   }
@@ -458,16 +509,19 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   p.s_begin = 0;
   p.s_end = p.P;
   p.status = d->status;
-  const size_t row_q = static_cast<size_t>(H) * D * 2;      // bytes per token of q, o
+  const size_t row_q = static_cast<size_t>(H) * D * 2;      // bytes per token of q
   const size_t row_kv = static_cast<size_t>(G) * D * 2;     // bytes per token of k, v
   const size_t w_q = static_cast<size_t>(hpg) * D * 2;      // a piece's bytes per token
+  const size_t o_elem = pr->o_dtype == RA_DTYPE_F32 ? 4 : 2;
+  const size_t row_o = static_cast<size_t>(H) * D * o_elem;  // the same for o
+  const size_t w_o = static_cast<size_t>(hpg) * D * o_elem;
   const size_t w_kv = static_cast<size_t>(D) * 2;
   const size_t lse_piece = static_cast<size_t>(hpg) * N * sizeof(float);
   // Tensors in page-locked memory mapped at the same address are moved by copy kernels
   // (hostcopy.cu); the rest by the copy engines.
   const size_t bq = static_cast<size_t>(B) * N * row_q, bkv = static_cast<size_t>(B) * N * row_kv;
   const bool zq = mapped_host(q, bq), zk = mapped_host(k, bkv), zv = mapped_host(v, bkv);
-  const bool zo = mapped_host(o, bq), zl = mapped_host(lse, static_cast<size_t>(B) * G * lse_piece);
+  const bool zo = mapped_host(o, static_cast<size_t>(B) * N * row_o), zl = mapped_host(lse, static_cast<size_t>(B) * G * lse_piece);
   // Outputs leave on a stream of this call's own, so a stalled output copy never holds
   // up the inputs (and the reverse); inputs come in on another stream of its own when
   // copy kernels move any of them, else on copy_stream. Streams of copy kernels run at
@@ -543,13 +597,13 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
     e = cudaEventRecord(ev_k(i), cs);
     // outputs of piece i out once its kernel is done
     if (e == cudaSuccess) e = cudaStreamWaitEvent(os, ev_k(i), 0);
-    uint8_t* od = static_cast<uint8_t*>(o) + static_cast<size_t>(b) * N * row_q + g * w_q;
+    uint8_t* od = static_cast<uint8_t*>(o) + static_cast<size_t>(b) * N * row_o + g * w_o;
     // lse [B, H, N]: the group's heads are consecutive rows
     uint8_t* ld = reinterpret_cast<uint8_t*>(lse) + (static_cast<size_t>(b) * G + g) * lse_piece;
     const int oblocks = i + 1 == n ? kCopyBlocksAlone : kCopyBlocks;
     if (e == cudaSuccess)
-      e = zo ? launch_rows_copy(od, row_q, p.o, w_q, w_q, N, oblocks, os)
-             : cudaMemcpy2DAsync(od, row_q, p.o, w_q, w_q, N, cudaMemcpyDeviceToHost, os);
+      e = zo ? launch_rows_copy(od, row_o, p.o, w_o, w_o, N, oblocks, os)
+             : cudaMemcpy2DAsync(od, row_o, p.o, w_o, w_o, N, cudaMemcpyDeviceToHost, os);
     if (e == cudaSuccess)
       e = zl ? launch_rows_copy(ld, lse_piece, p.lse, lse_piece, lse_piece, 1, oblocks, os)
              : cudaMemcpyAsync(ld, p.lse, lse_piece, cudaMemcpyDeviceToHost, os);
@@ -640,7 +694,7 @@ ra_status ring_attn_finalize(const ra_problem* pr, const float* m, const float* 
   if (!aligned16(m) || !aligned16(z) || !aligned16(y) || !aligned16(o) || !aligned16(lse))
     return RA_ERR_INVALID_ARG;
   const Bytes b = tensor_bytes(pr);
-  if (!writes_disjoint({{o, b.q}, {lse, b.rows}}, {{m, b.rows}, {z, b.rows}, {y, b.y}}))
+  if (!writes_disjoint({{o, b.o}, {lse, b.rows}}, {{m, b.rows}, {z, b.rows}, {y, b.y}}))
     return RA_ERR_INVALID_ARG;
   if (static_cast<long long>(pr->batch) > 65535 || pr->heads > 65535) return RA_ERR_UNSUPPORTED;
   DevInfo* d = nullptr;
@@ -680,7 +734,7 @@ ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_
   if (st != RA_OK) return st;
   if ((st = resident(d, {o_parts, lse_parts, o, lse})) != RA_OK) return st;
   return launch_result(launch_merge(n_parts, batch, seqlen, heads, head_dim, o_parts, lse_parts,
-                                    o, lse, static_cast<cudaStream_t>(stream)));
+                                    o, false, lse, static_cast<cudaStream_t>(stream)));
 }
 
 ra_status ring_attn_shard_map(int32_t layout, int32_t seqlen, int32_t P, int32_t* owner,
@@ -756,7 +810,7 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
   {
     const Bytes b = tensor_bytes(pr);
     if (!writes_disjoint({{dq, b.q}, {dk, b.kv}, {dv, b.kv}, {workspace, bwd_workspace(pr)}},
-                         {{q, b.q}, {k, b.kv}, {v, b.kv}, {o, b.q}, {lse, b.rows}, {dout, b.q}}))
+                         {{q, b.q}, {k, b.kv}, {v, b.kv}, {o, b.o}, {lse, b.rows}, {dout, b.q}}))
       return RA_ERR_INVALID_ARG;
   }
   // the extension rows are addressed by 32-bit TMA coordinates
@@ -781,6 +835,7 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
   p.L = f.L;
   p.nt = f.nq;
   p.tiles = static_cast<int32_t>(bwd_tiles(pr));
+  p.o_f32 = f.o_f32;
   p.scale = f.scale;
   p.scale_log2 = f.scale_log2;
   p.timeout_ns = f.timeout_ns;
@@ -826,7 +881,8 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
   {
     const Bytes b = tensor_bytes(pr);
     const size_t qrows = static_cast<size_t>(pr->batch) * n_q * pr->heads;
-    if (!writes_disjoint({{o, qrows * pr->head_dim * 2}, {lse, qrows * sizeof(float)},
+    const size_t o_elem = pr->o_dtype == RA_DTYPE_F32 ? 4 : 2;
+    if (!writes_disjoint({{o, qrows * pr->head_dim * o_elem}, {lse, qrows * sizeof(float)},
                           {workspace, decode_workspace(pr, n_q)}},
                          {{q, qrows * pr->head_dim * 2}, {k, b.kv}, {v, b.kv}}))
       return RA_ERR_INVALID_ARG;
@@ -857,7 +913,8 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
   cudaError_t e = launch_decode_partials(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, cs);
   if (e != cudaSuccess) return RA_ERR_CUDA;
   return launch_result(launch_merge(static_cast<int>(parts), pr->batch, n_q, pr->heads,
-                                    pr->head_dim, o_parts, lse_parts, o, lse, cs));
+                                    pr->head_dim, o_parts, lse_parts, o, p.o_f32 != 0, lse,
+                                    cs));
 }
 
 ra_status ring_attn_last_error(int32_t* device_code) {
@@ -870,6 +927,12 @@ ra_status ring_attn_last_error(int32_t* device_code) {
   if (cudaMemcpyFromSymbol(&code, g_status, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
   if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
   *device_code = code;
+  return RA_OK;
+}
+
+ra_status ring_attn_selftest_wait_limit(uint64_t limit_ns) {
+  if (limit_ns > kWaitLimitNs) return RA_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : limit_ns);
   return RA_OK;
 }
 

@@ -241,17 +241,31 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
     const size_t li = (static_cast<size_t>(bat) * p.H + h) * p.N + pos;
     if (valid && in_bounds(off, 8, q_elems(p), p.status) &&
         in_bounds(li, 1, row_elems(p), p.status)) {
-      const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + off);
       const uint4 b =
           *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + off);
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w};
       const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+      float ov[8];
+      if (p.o_f32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.o) + off);
+        const float4 a0 = src[0], a1 = src[1];
+        ov[0] = a0.x; ov[1] = a0.y; ov[2] = a0.z; ov[3] = a0.w;
+        ov[4] = a1.x; ov[5] = a1.y; ov[6] = a1.z; ov[7] = a1.w;
+      } else {
+        const uint4 a =
+            *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + off);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+          ov[2 * e] = fa.x;
+          ov[2 * e + 1] = fa.y;
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
         const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
-        dsum = fmaf(fa.x, fb.x, dsum);
-        dsum = fmaf(fa.y, fb.y, dsum);
+        dsum = fmaf(ov[2 * e], fb.x, dsum);
+        dsum = fmaf(ov[2 * e + 1], fb.y, dsum);
       }
       const float l = p.lse[li];
       l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;   // a row with no key contributes 0
@@ -599,6 +613,9 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     const uint32_t tS = tmem + kColS + lane_off + half * 64;
     const uint32_t tDP = tmem + kColDP + lane_off + half * 64;
     const float2 cc = make_float2(p.scale_log2, p.scale_log2);
+    // First local query row of the current query segment that sees this key (kept per
+    // segment, so the striped layout divides by its stride once per segment, not per tile).
+    int seg_key = -1, first_q = 0;
     bool ok = true;
     walk_qtiles<ZIG>(p, w, [&](int t, int, const Seg& sq, int qt) {
       const uint32_t par = static_cast<uint32_t>(t) & 1;
@@ -624,9 +641,11 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       // of the tile's columns. (Columns past the chunk's end hold -1e30 there.)
       int cf = 0;
       if (p.causal) {
-        const int q0 = sq.base + qt * 128 * sq.stride;
-        cf = kpos <= q0 ? 0 : min(128, (kpos - q0 + sq.stride - 1) / sq.stride);
-        cf -= half * 64;
+        if (sq.base != seg_key) {
+          seg_key = sq.base;
+          first_q = kpos <= sq.base ? 0 : (kpos - sq.base + sq.stride - 1) / sq.stride;
+        }
+        cf = min(max(first_q - qt * 128, 0), 128) - half * 64;
       }
       if (__any_sync(0xffffffffu, cf > 0)) {
 #pragma unroll
@@ -980,9 +999,15 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarFix));
     }
+    // this row's visible keys of the current key segment, a prefix (kept per segment)
+    int seg_key = -1, row_vis = 0;
     bool ok = true;
     walk_ktiles<ZIG>(p, w, [&](int t, const Seg& sk, int kt) {
       const uint32_t par = static_cast<uint32_t>(t) & 1;
+      if (sk.base != seg_key || kt == 0) {
+        seg_key = sk.base;
+        row_vis = seg_visible(sk, p.causal, 0, sk.len, qpos);
+      }
       if (!__all_sync(0xffffffffu, bounded_wait(bar(kSF), par, p.timeout_ns, abort_flag))) {
         ok = false;
         return false;
@@ -1003,7 +1028,7 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kW1));
       // causal / segment-tail mask: the visible keys of the tile are a prefix
-      const int cnt = seg_visible(sk, p.causal, kt * 128, 128, qpos) - half * 64;
+      const int cnt = min(max(row_vis - kt * 128, 0), 128) - half * 64;
       if (__any_sync(0xffffffffu, cnt < 64)) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
@@ -1069,24 +1094,18 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
   }
 }
 
-// Sets the dynamic shared-memory limit of a kernel once per device.
+// Sets the dynamic shared-memory limit of a kernel once per device context.
 template <typename K>
-cudaError_t set_smem_once(K kernel, int bytes, std::atomic<unsigned long long>& done) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (done.load() & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.fetch_or(bit);
-  return e;
+cudaError_t set_smem_once(K kernel, int bytes, OncePerContext& once) {
+  return once.run(
+      [&] { return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
 }
 
 template <int D, bool ZIG>
 cudaError_t launch_dkdv_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& text,
                           cudaStream_t st) {
-  static std::atomic<unsigned long long> done{0};
+  static OncePerContext done;
   const int smem = BwdSmem<D>::kAlloc;
   cudaError_t e = set_smem_once(bwd_dkdv_kernel<D, ZIG>, smem, done);
   if (e != cudaSuccess) return e;
@@ -1100,7 +1119,7 @@ cudaError_t launch_dkdv_d(const BwdParams& p, const CUtensorMap& tq, const CUten
 template <int D, bool ZIG>
 cudaError_t launch_dq_d(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                         const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-  static std::atomic<unsigned long long> done{0};
+  static OncePerContext done;
   const int smem = DqSmem<D>::kAlloc;
   cudaError_t e = set_smem_once(bwd_dq_kernel<D, ZIG>, smem, done);
   if (e != cudaSuccess) return e;

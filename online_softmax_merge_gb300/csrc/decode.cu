@@ -355,19 +355,14 @@ cudaError_t launch_d(const RingParams& p, const CUtensorMap& tk, const CUtensorM
   const int chunk = decode_chunk_keys(p.S, p.P, p.layout);
   const int n_chunks = (seg_len + chunk - 1) / chunk;
   const int smem = DecSmem<D>::kAlloc;
-  // the shared-memory limit is set once per device (a decode loop calls this per token,
-  // possibly inside a CUDA graph capture)
-  static std::atomic<unsigned long long> attr_done{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // the shared-memory limit is set once per device context (a decode loop calls this per
+  // token, possibly inside a CUDA graph capture)
+  static OncePerContext attr;
+  const cudaError_t e = attr.run([&] {
+    return cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem);
+  });
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_done.load() & bit)) {
-    e = cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit);
-  }
   const dim3 grid(p.G * n_rowgroups, nseg * n_chunks, p.B * p.P);
   decode_mma_kernel<D><<<grid, kThreads, smem, st>>>(p, tk, tv, n_q, q_pos0, chunk, n_rowgroups,
                                                      n_chunks, o_parts, lse_parts);

@@ -10,11 +10,15 @@
 // front. Such callers still pass q, k, v, o and lse; only the scratch for the
 // partials comes from here, so the call itself allocates nothing.
 //
-// The price: the array (kScratchBytes) is static device memory, reserved on every
-// GPU that loads this library and held until the process exits; problems whose
-// partials need more than that are rejected; and because every call on a GPU
-// shares the one array, calls whose kernels overlap on that GPU (different
-// streams, no ordering between them) race on it.
+// The price: the array (kScratchBytes) is static device memory, held until the
+// process exits by every GPU on which this file's module has been loaded. The CUDA
+// runtime loads modules lazily by default, so that happens at the first call of this
+// entry point on a device (the lookup of the array's address below): that first
+// call reserves the array, can fail with RA_ERR_CUDA if the device has no room for
+// it, and should come before any stream capture; later calls allocate nothing.
+// Problems whose partials need more than the array are rejected; and because every
+// call on a GPU shares the one array, calls whose kernels overlap on that GPU
+// (different streams, no ordering between them) race on it.
 #include <mutex>
 
 #include "internal.cuh"
@@ -31,23 +35,34 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx = 0;   // context the address belongs to (0: not looked up)
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of the scratch array in the current context, looked up (with the
+// device current) the first time and again whenever the context is a new one.
 cudaError_t scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (a.ptr == nullptr || id == 0 || a.ctx != id) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = ptr;
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();   // leave no error behind for the caller's next CUDA call
+      a.ptr = nullptr;
+      return e;
+    }
+    a.ptr = ptr;
+    a.ctx = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = a.ptr;
   return cudaSuccess;
 }
 

@@ -46,18 +46,17 @@ bool multiple(uintptr_t x, uintptr_t m) { return x % m == 0; }
 cudaError_t launch_rows_copy(void* dst, size_t dpitch, const void* src, size_t spitch,
                              size_t width, size_t rows, int blocks, cudaStream_t st) {
   // No shared memory: prefer the split that lets these blocks sit beside others. A
-  // preference only, set once per device (one bit per ordinal; callers may be threads).
-  static std::atomic<unsigned long long> carveout_done{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(carveout_done.load() & bit)) {
-      cudaFuncSetAttribute(rows_copy<uint4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-      cudaFuncSetAttribute(rows_copy<uint32_t>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           100);
-      carveout_done.fetch_or(bit);
-    }
-  }
+  // preference only (its failure is ignored), set once per device context.
+  static OncePerContext carveout;
+  (void)carveout.run([] {
+    cudaError_t r =
+        cudaFuncSetAttribute(rows_copy<uint4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(rows_copy<uint32_t>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               100);
+    if (r != cudaSuccess) (void)cudaGetLastError();
+    return r;
+  });
   const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) |
                       static_cast<uintptr_t>(dpitch) | static_cast<uintptr_t>(spitch) |
                       static_cast<uintptr_t>(width);

@@ -4,9 +4,43 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/ringattn.h"
 
 namespace ra {
+
+// Id of the CUDA context current on the calling thread (the driver's cuCtxGetId,
+// unique within the process), or 0 when no context is current or the driver cannot
+// say. What the library looks up once and keeps per device -- the device addresses
+// of its static arrays, the kernels' shared-memory limits -- is remembered together
+// with this id and looked up again when it changes: an application that destroys a
+// device's context and makes a new one (cudaDeviceReset, then further calls) would
+// otherwise launch kernels with addresses and limits that belong to the old one.
+unsigned long long current_context_id();
+
+// A one-time setting (a kernel attribute), made once in every context of a device
+// and again whenever the current context is a new one.
+class OncePerContext {
+ public:
+  template <typename F>
+  cudaError_t run(F&& set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::atomic<unsigned long long>& done = done_[dev & 63];  // a shared slot only costs a redo
+    const unsigned long long id = current_context_id();
+    if (id != 0 && done.load() == id) return cudaSuccess;
+    e = set();
+    if (e != cudaSuccess) return e;
+    const unsigned long long now = current_context_id();    // setting it made one current
+    if (now != 0) done.store(now);
+    return cudaSuccess;
+  }
+
+ private:
+  std::atomic<unsigned long long> done_[64] = {};
+};
 
 // Debug builds (compiled with -DRA_DEBUG): every raw global access (one that is not
 // a TMA copy, which the hardware bounds by its tensor map) first checks its element
@@ -60,6 +94,7 @@ struct RingParams {
   int32_t s_begin, s_end;
   int32_t step_mode;      // 0: fold all steps then write O, LSE; 1: read/write (m, z, y)
   int32_t load_state;     // step mode: 1 = start from the HBM state, 0 = from empty
+  int32_t o_f32;          // o is fp32 (RA_DTYPE_F32) instead of bf16
   float scale;            // score scale (natural units)
   float scale_log2;       // scale * log2(e)
   uint64_t timeout_ns;    // limit of every device-side wait
@@ -82,6 +117,7 @@ struct BwdParams {
   int32_t B, N, H, G, D, S, P, layout, causal;
   int32_t X, L, nt;
   int32_t tiles;          // B * H * X * nt query tiles
+  int32_t o_f32;          // the saved o is fp32 (RA_DTYPE_F32) instead of bf16
   float scale;            // score scale (natural units)
   float scale_log2;       // scale * log2(e)
   uint64_t timeout_ns;    // limit of every device-side wait
@@ -108,7 +144,8 @@ cudaError_t launch_ring_tc(const RingParams& p, const CUtensorMap& tq, const CUt
 cudaError_t launch_ring_simt(const RingParams& p, cudaStream_t st);
 cudaError_t launch_finalize(const RingParams& p, cudaStream_t st);
 cudaError_t launch_merge(int n, int B, int N, int H, int D, const float* o_parts,
-                         const float* lse_parts, void* o, float* lse, cudaStream_t st);
+                         const float* lse_parts, void* o, bool o_f32, float* lse,
+                         cudaStream_t st);
 cudaError_t launch_shard_map(int layout, int N, int P, int32_t* owner, int32_t* local,
                              int32_t* token_of, cudaStream_t st);
 cudaError_t launch_tile_classes(const RingParams& p, int u, int b, int8_t* classes,

@@ -47,10 +47,30 @@ __device__ __forceinline__ void load_vec(const float2* p, float (&r)[2]) {
   r[0] = v.x; r[1] = v.y;
 }
 
-template <int D>
+// One lane's kN consecutive output values: rounded to bf16 (round to nearest
+// even), or kept as fp32.
+__device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float (&a)[4]) {
+  __nv_bfloat162 x = __floats2bfloat162_rn(a[0], a[1]);
+  __nv_bfloat162 y = __floats2bfloat162_rn(a[2], a[3]);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&x);
+  pk.y = *reinterpret_cast<uint32_t*>(&y);
+  *reinterpret_cast<uint2*>(dst) = pk;
+}
+__device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float (&a)[2]) {
+  *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(a[0], a[1]);
+}
+__device__ __forceinline__ void store_out(float* dst, const float (&a)[4]) {
+  *reinterpret_cast<float4*>(dst) = make_float4(a[0], a[1], a[2], a[3]);
+}
+__device__ __forceinline__ void store_out(float* dst, const float (&a)[2]) {
+  *reinterpret_cast<float2*>(dst) = make_float2(a[0], a[1]);
+}
+
+template <int D, typename OutT>
 __global__ void __launch_bounds__(kWarps * 32)
 merge_kernel(int n, int B, int N, int H, const float* __restrict__ o_parts,
-             const float* __restrict__ lse_parts, __nv_bfloat16* __restrict__ o,
+             const float* __restrict__ lse_parts, OutT* __restrict__ o,
              float* __restrict__ lse) {
   using V = Vec<D>;
   constexpr int kN = V::kN;
@@ -137,27 +157,16 @@ merge_kernel(int n, int B, int N, int H, const float* __restrict__ o_parts,
         for (int e = 0; e < kN; ++e) acc[e] = fmaf(wgt, r[e], acc[e]);
       }
     }
-    __nv_bfloat16* dst = o + orow + lane * kN;
-    if (kN == 4) {
-      __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
-      __nv_bfloat162 b = __floats2bfloat162_rn(acc[kN - 2], acc[kN - 1]);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&a);
-      pk.y = *reinterpret_cast<uint32_t*>(&b);
-      *reinterpret_cast<uint2*>(dst) = pk;
-    } else {
-      __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
-      *reinterpret_cast<__nv_bfloat162*>(dst) = a;
-    }
+    store_out(o + orow + lane * kN, acc);
   }
 }
 
-// (m, z, y) -> O = y / z (bf16), LSE = m + ln z; z = 0 gives O = 0, LSE = -inf.
-template <int D>
+// (m, z, y) -> O = y / z (bf16 or fp32), LSE = m + ln z; z = 0 gives O = 0,
+// LSE = -inf.
+template <int D, typename OutT>
 __global__ void __launch_bounds__(kWarps * 32)
 finalize_kernel(int N, int H, const float* __restrict__ m, const float* __restrict__ z,
-                const float* __restrict__ y, __nv_bfloat16* __restrict__ o,
-                float* __restrict__ lse) {
+                const float* __restrict__ y, OutT* __restrict__ o, float* __restrict__ lse) {
   using V = Vec<D>;
   constexpr int kN = V::kN;
   __shared__ float s_inv[kTok];
@@ -185,41 +194,46 @@ finalize_kernel(int N, int H, const float* __restrict__ m, const float* __restri
     const size_t orow = ((static_cast<size_t>(bat) * N + t) * H + head) * D;
     float r[kN];
     load_vec(reinterpret_cast<const typename V::T*>(y + orow) + lane, r);
-    __nv_bfloat16* dst = o + orow + lane * kN;
-    if (kN == 4) {
-      __nv_bfloat162 a = __floats2bfloat162_rn(r[0] * inv, r[1] * inv);
-      __nv_bfloat162 b = __floats2bfloat162_rn(r[kN - 2] * inv, r[kN - 1] * inv);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&a);
-      pk.y = *reinterpret_cast<uint32_t*>(&b);
-      *reinterpret_cast<uint2*>(dst) = pk;
-    } else {
-      __nv_bfloat162 a = __floats2bfloat162_rn(r[0] * inv, r[1] * inv);
-      *reinterpret_cast<__nv_bfloat162*>(dst) = a;
-    }
+#pragma unroll
+    for (int e = 0; e < kN; ++e) r[e] *= inv;
+    store_out(o + orow + lane * kN, r);
   }
+}
+
+template <int D, typename OutT>
+void merge_d(int n, int B, int N, int H, const float* o_parts, const float* lse_parts, void* o,
+             float* lse, cudaStream_t st) {
+  const dim3 grid((N + kTok - 1) / kTok, H, B);
+  merge_kernel<D, OutT><<<grid, kWarps * 32, 0, st>>>(n, B, N, H, o_parts, lse_parts,
+                                                      static_cast<OutT*>(o), lse);
+}
+
+template <int D, typename OutT>
+void finalize_d(const RingParams& p, cudaStream_t st) {
+  const dim3 grid((p.N + kTok - 1) / kTok, p.H, p.B);
+  finalize_kernel<D, OutT><<<grid, kWarps * 32, 0, st>>>(p.N, p.H, p.m, p.z, p.y,
+                                                         static_cast<OutT*>(p.o), p.lse);
 }
 
 }  // namespace
 
 cudaError_t launch_merge(int n, int B, int N, int H, int D, const float* o_parts,
-                         const float* lse_parts, void* o, float* lse, cudaStream_t st) {
-  const dim3 grid((N + kTok - 1) / kTok, H, B);
-  auto* ob = static_cast<__nv_bfloat16*>(o);
+                         const float* lse_parts, void* o, bool o_f32, float* lse,
+                         cudaStream_t st) {
   if (D == 64)
-    merge_kernel<64><<<grid, kWarps * 32, 0, st>>>(n, B, N, H, o_parts, lse_parts, ob, lse);
+    o_f32 ? merge_d<64, float>(n, B, N, H, o_parts, lse_parts, o, lse, st)
+          : merge_d<64, __nv_bfloat16>(n, B, N, H, o_parts, lse_parts, o, lse, st);
   else
-    merge_kernel<128><<<grid, kWarps * 32, 0, st>>>(n, B, N, H, o_parts, lse_parts, ob, lse);
+    o_f32 ? merge_d<128, float>(n, B, N, H, o_parts, lse_parts, o, lse, st)
+          : merge_d<128, __nv_bfloat16>(n, B, N, H, o_parts, lse_parts, o, lse, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const RingParams& p, cudaStream_t st) {
-  const dim3 grid((p.N + kTok - 1) / kTok, p.H, p.B);
-  auto* ob = static_cast<__nv_bfloat16*>(p.o);
   if (p.D == 64)
-    finalize_kernel<64><<<grid, kWarps * 32, 0, st>>>(p.N, p.H, p.m, p.z, p.y, ob, p.lse);
+    p.o_f32 ? finalize_d<64, float>(p, st) : finalize_d<64, __nv_bfloat16>(p, st);
   else
-    finalize_kernel<128><<<grid, kWarps * 32, 0, st>>>(p.N, p.H, p.m, p.z, p.y, ob, p.lse);
+    p.o_f32 ? finalize_d<128, float>(p, st) : finalize_d<128, __nv_bfloat16>(p, st);
   return cudaGetLastError();
 }
 

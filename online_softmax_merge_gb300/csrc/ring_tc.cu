@@ -581,6 +581,9 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
       for (int ks = 0; ks < (ZIG ? 2 : 1) && ok; ++ks) {
         const Seg sk = seg_of(p.layout, p.S, p.P, b, ks);
         const int nk = kv_tiles(p, sk, w.qpos_max);
+        // this row's visible keys of the segment, a prefix (one division per segment
+        // rather than per tile in the striped layout)
+        const int row_vis = seg_visible(sk, p.causal, 0, sk.len, qpos);
         for (int kt = 0; kt < nk; ++kt, ++t) {
           // this tile's scores: buffer i at d = 128; buffer (2t + i) mod 3 at d = 64
           const int kseq = 2 * t + i;
@@ -601,7 +604,7 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
             for (int j = 0; j < 128; ++j) sc[j] = __uint_as_float(r[j]);
           }
           // Causal and segment-tail mask: the visible keys of this tile are a prefix.
-          const int cnt = seg_visible(sk, p.causal, kt * 128, 128, qpos);
+          const int cnt = min(max(row_vis - kt * 128, 0), 128);
           if (__any_sync(0xffffffffu, cnt < 128)) {
   #pragma unroll
             for (int c = 0; c < 128; ++c)
@@ -718,7 +721,14 @@ ring_tc_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUt
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld_x32(tO + c * 32, r);
-          if (io_ok) {
+          if (io_ok && p.o_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + yo + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
+                                   __uint_as_float(r[4 * j + 2]) * inv,
+                                   __uint_as_float(r[4 * j + 3]) * inv);
+          } else if (io_ok) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + yo + c * 32);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -765,20 +775,16 @@ template <int D>
 cudaError_t launch_d(const RingParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t st) {
   const int smem = Smem<D>::kAlloc;
-  static std::atomic<unsigned long long> attr_done{0};   // one bit per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_done.load() & bit)) {
-    e = cudaFuncSetAttribute(ring_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(ring_tc_kernel<D, true>,
+  static OncePerContext attr;   // the limit belongs to the device's current context
+  cudaError_t e = attr.run([&] {
+    cudaError_t r = cudaFuncSetAttribute(ring_tc_kernel<D, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(ring_tc_kernel<D, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit);
-  }
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(p.B) * p.G * p.units_per_bg;
   if (grid <= 0) return cudaSuccess;
   if (p.layout == kZigzag)

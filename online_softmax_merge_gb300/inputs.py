@@ -103,13 +103,24 @@ def make_qkv(w: Workload, device="cpu", seed: Optional[int] = None):
     k = k.to(torch.bfloat16)
     v = v.to(torch.bfloat16)
     if w.stress_frac > 0.0:
-        gs = torch.Generator(device="cpu")
-        gs.manual_seed(seed + 1)
-        n_rows = max(1, int(round(w.stress_frac * N)))
-        for b in range(B):
-            rows = torch.randperm(N, generator=gs)[:n_rows].to(dev)
+        for b, rows in enumerate(stress_positions(w, seed)):
+            rows = rows.to(dev)
             k[b, rows] = k[b, rows] * w.stress_factor
     return q, k, v
+
+
+def stress_positions(w: Workload, seed: Optional[int] = None):
+    """Per batch, the token positions whose K rows make_qkv multiplies by
+    stress_factor: the first round(stress_frac * N) entries of a random permutation
+    of the N positions, drawn batch after batch from a CPU generator seeded seed+1
+    (seed defaults to the workload's). Empty tensors when the workload has none."""
+    seed = w.seed if seed is None else seed
+    if w.stress_frac <= 0.0:
+        return [torch.empty(0, dtype=torch.int64) for _ in range(w.batch)]
+    gs = torch.Generator(device="cpu")
+    gs.manual_seed(seed + 1)
+    n_rows = max(1, int(round(w.stress_frac * w.seqlen)))
+    return [torch.randperm(w.seqlen, generator=gs)[:n_rows] for _ in range(w.batch)]
 
 
 def make_dout(w: Workload, device="cpu", seed: Optional[int] = None):

@@ -53,6 +53,7 @@ int main(int argc, char** argv) {
   p.causal = atoi(argv[8]);
   p.layout = atoi(argv[9]);
   p.scale = 0.f;
+  p.o_dtype = RA_DTYPE_BF16;
   const size_t tok = (size_t)p.batch * (size_t)p.seqlen;
   const size_t bq = tok * (size_t)p.heads * (size_t)p.head_dim * 2;
   const size_t bkv = tok * (size_t)p.kv_heads * (size_t)p.head_dim * 2;

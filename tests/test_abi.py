@@ -50,6 +50,14 @@ def test_debug_build_exports_the_same_symbols_and_reports_its_checks(lib):
         assert lib.ring_attn_debug_checks() == 0
 
 
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define RA_DECODE_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m is not None
+    assert _lib.RA_DECODE_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+    assert re.search(r"#define RA_TILE %d\b" % _lib.TILE, text)
+
+
 def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert lib.ra_status_str(code).decode() == name
@@ -264,3 +272,27 @@ def test_written_ranges_may_not_overlap_other_arguments(lib):
     assert _no_device_reached(host(q, k, v, o, lse, ws))
     assert host(q, k, v, o, lse, _at(3, 256)) == _lib.RA_ERR_INVALID_ARG    # workspace over o
     assert host(q, k, v, o, _at(2), ws) == _lib.RA_ERR_INVALID_ARG          # lse = v
+
+
+def test_fp32_output_ranges_and_bad_dtype(lib):
+    """With o_dtype = RA_DTYPE_F32 the written range of o is 4 bytes per element, so
+    a range that clears a bf16 o may overlap as fp32; any other o_dtype is refused."""
+    pr = _pr(o_dtype=_lib.RA_DTYPE_F32)             # B=1 N=256 H=4 G=2 d=128
+    bq = 256 * 4 * 128 * 2
+    q, k, v, o = (_at(i) for i in range(4))
+    fwd = lambda p, *a: lib.ring_attn_fwd(ctypes.byref(p), *a, None)
+    assert _no_device_reached(fwd(pr, q, k, v, o, _at(3, 2 * bq)))       # lse right after o
+    assert fwd(pr, q, k, v, o, _at(3, bq)) == _lib.RA_ERR_INVALID_ARG    # lse inside fp32 o
+    assert _no_device_reached(fwd(_pr(), q, k, v, o, _at(3, bq)))       # ... but after bf16 o
+    bad = _pr(o_dtype=2)
+    assert fwd(bad, q, k, v, o, _at(4)) == _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_finalize(ctypes.byref(bad), q, k, v, o, _at(4), None) == \
+        _lib.RA_ERR_INVALID_ARG
+
+
+def test_selftest_wait_limit_is_host_only_and_checked(lib):
+    """The abort-path test hook only sets the limit later launches get."""
+    assert lib.ring_attn_selftest_wait_limit(ctypes.c_uint64(3_000_000_000)) == \
+        _lib.RA_ERR_INVALID_ARG
+    assert lib.ring_attn_selftest_wait_limit(ctypes.c_uint64(5)) == _lib.RA_OK
+    assert lib.ring_attn_selftest_wait_limit(ctypes.c_uint64(0)) == _lib.RA_OK

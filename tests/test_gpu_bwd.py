@@ -98,6 +98,19 @@ def test_bwd_after_gpu_forward(w):
         assert_close(host32(got), r, name)
 
 
+@pytest.mark.parametrize("w", [CASES[1], CASES[3], CASES[8]], ids=["striped", "zigzag-d64", "stress"])
+def test_bwd_from_fp32_forward_output(w):
+    """The saved O may be the forward's fp32 output (RA_DTYPE_F32): the statistics
+    pass reads it as fp32."""
+    q, k, v, do = _inputs(w)
+    o, lse = ra.fwd(q, k, v, w.P, w.layout, w.causal, out_dtype=torch.float32)
+    dq, dk, dv = _bwd(w, q, k, v, o, lse, do)
+    hq, hk, hv, hdo = (host32(t).astype(np.float64) for t in (q, k, v, do))
+    ref = OB.attention_grads(hq, hk, hv, hdo, w.causal)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        assert_close(host32(got), r, name)
+
+
 def test_bwd_layouts_agree_and_runs_are_deterministic():
     w = Workload("gqa", 1, 8 * (128 + 84), 4, 2, 128, 4, "contiguous", True, 210)
     q, k, v, do = _inputs(w)

@@ -87,3 +87,25 @@ def test_decode_equals_fused_forward_rows():
     torch.cuda.synchronize()
     assert float((od.float() - of[:, -n_q:].float()).abs().max()) <= 2 * TOL_O
     assert float((ld - lf[:, :, -n_q:]).abs().max()) <= 2 * TOL_LSE
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[7]], ids=["striped", "zigzag"])
+def test_decode_fp32_output(case):
+    """Decode with O written as fp32 by the merge kernel: within the bar of the
+    oracle, and its bf16 rounding is the bf16 call's output."""
+    B, N, H, G, d, P, layout, causal, n_q, q_pos0 = case
+    if q_pos0 is None:
+        q_pos0 = N - n_q
+    w = Workload("dec32", B, N, H, G, d, P, layout, causal, seed=350)
+    _, k, v = (t.to(DEV) for t in make_qkv(w))
+    g = torch.Generator().manual_seed(19)
+    q = torch.randn((B, n_q, H, d), generator=g).to(torch.bfloat16).to(DEV)
+    o32, l32 = ra.decode(q, k, v, P, q_pos0, layout, causal, out_dtype=torch.float32)
+    o16, l16 = ra.decode(q, k, v, P, q_pos0, layout, causal)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    assert torch.equal(o16, o32.to(torch.bfloat16)) and torch.equal(l16, l32)
+    rows = np.arange(q_pos0, q_pos0 + n_q)
+    O_ref, L_ref = attention_at(host32(q), rows, list(range(H)), H, host32(k), host32(v), causal)
+    assert float(np.abs(host32(o32) - O_ref).max()) <= TOL_O
+    assert float(np.abs(host32(l32) - L_ref).max()) <= TOL_LSE

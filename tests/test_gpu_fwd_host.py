@@ -162,3 +162,23 @@ def test_host_mapped_refuses_a_range_with_an_unmapped_hole():
             cr.cudaHostUnregister(a0)
         if r2 == 0:
             cr.cudaHostUnregister(a0 + 4 * MB)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_forward_fp32_output_equals_device_forward(pinned):
+    """O written as fp32 into host memory (pieces' strided output copies of 4-byte
+    elements) equals the device forward's fp32 output bit for bit."""
+    w = Workload("host32", 2, 4 * (128 + 40), 4, 2, 128, 4, "striped", True, 430)
+    q, k, v = make_qkv(w)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o_h, l_h = ra.fwd_host(q, k, v, w.P, w.layout, w.causal, device=DEV,
+                           out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    assert o_h.dtype == torch.float32 and o_h.device.type == "cpu"
+    o_d, l_d = ra.fwd(q.to(DEV), k.to(DEV), v.to(DEV), w.P, w.layout, w.causal,
+                      out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    assert torch.equal(l_h, l_d.cpu())

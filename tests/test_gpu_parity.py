@@ -176,3 +176,21 @@ def test_large_logits_stay_within_the_arithmetic_bounds(factor):
     eo = float(np.abs(host32(o) - O).max())
     assert el <= 2.0 ** -21 * dot_mag + 1e-6, (el, dot_mag)
     assert eo <= 2.0 ** -9 * float(np.abs(hv).max()) + 2.0 ** -8 * float(np.abs(O).max()) + 1e-4, eo
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fwd_fp32_output(case):
+    """O written as fp32 (RA_DTYPE_F32): within the bar of the oracle, and the bf16
+    output of the same call is exactly its rounding to nearest even (one
+    computation, two stores)."""
+    name, B, N, H, G, d, P, layout, causal = case
+    w = Workload(name, B, N, H, G, d, P, layout, causal, seed=100 + CASES.index(case))
+    q, k, v, o16, l16 = _run(w)
+    o32, l32 = ra.fwd(q, k, v, P, layout, causal, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert ra.last_error(DEV) == 0
+    assert o32.dtype == torch.float32
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(l16, l32)
+    eo, el = compare_full(o32, l32, q, k, v, causal)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)

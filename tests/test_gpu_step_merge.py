@@ -173,3 +173,37 @@ def test_gpu_shard_partials_merge_to_fused_forward():
     torch.cuda.synchronize()
     assert float((o.float() - of.float()).abs().max()) <= 2 * TOL_O
     assert float((lse - lf).abs().max()) <= 2 * TOL_LSE
+
+
+def test_finalize_fp32_output_matches_oracle():
+    g = torch.Generator().manual_seed(31)
+    B, N, H, d = 1, 70, 2, 64
+    m = torch.randn((B, H, N), generator=g)
+    z = torch.rand((B, H, N), generator=g) * 5 + 0.5
+    z[0, 0, :3] = 0.0
+    m[0, 0, :3] = -float("inf")
+    y = torch.randn((B, N, H, d), generator=g) * 3
+    st = (m.to(DEV), z.to(DEV), y.to(DEV))
+    o32, l32 = ra.finalize(st, out_dtype=torch.float32)
+    o16, l16 = ra.finalize(st)
+    torch.cuda.synchronize()
+    Ow, _ = OM.finalize(m.double().numpy(), z.double().numpy(), y.double().numpy())
+    # y * (1/z) in fp32: two roundings of 2^-24 each
+    assert np.all(np.abs(host32(o32) - Ow) <= 2.0 ** -22 * np.abs(Ow) + 1e-30)
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(l16, l32)
+
+
+def test_step_path_fp32_finalize_equals_fused_fp32_forward():
+    w = Workload("sf32", 1, 4 * 200, 4, 2, 128, 4, "striped", True, 32)
+    q, k, v = _inputs(w)
+    st = ra.empty_state(q)
+    for s in range(w.P):
+        ra.step(q, k, v, w.P, s, st, first=(s == 0), layout=w.layout, causal=True)
+    o, lse = ra.finalize(st, w.P, w.layout, out_dtype=torch.float32)
+    of, lf = ra.fwd(q, k, v, w.P, w.layout, True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    eo, el = compare_full(o, lse, q, k, v, True)
+    assert eo <= TOL_O and el <= TOL_LSE, (eo, el)
+    # same fp32 recurrence, different summation order
+    assert float((o - of).abs().max()) <= 1e-3
