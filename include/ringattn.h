@@ -353,12 +353,17 @@ ra_status ring_attn_selftest_timeout(uint64_t limit_ns, void* stream);
 /* Test hook for the kernels' abort path. Sets the time limit of every device-side
  * wait of the forward, step, backward and decode kernels launched by later calls
  * in this process (all devices) to limit_ns nanoseconds; 0 restores the default,
- * 2 s. A limit of a few nanoseconds makes real waits of those kernels run out on
- * an ordinary problem: the kernel that gives up records RA_ERR_TIMEOUT, stops its
- * other roles through a shared flag, lets the copies and products it has in flight
- * finish (those waits keep their own fixed limit), frees its tensor memory and
- * returns, and its outputs are undefined. Meant for tests only: an application has
- * no reason to call it. Limits above the default give RA_ERR_INVALID_ARG. */
+ * 2 s. In the debug build (ring_attn_debug_checks() == 1) every wait tests its
+ * barrier without blocking and looks at its limit on every poll (a limit under
+ * 1000 ns, below the resolution of the GPU's timer, counts polls), so a limit of a
+ * few nanoseconds makes every wait that is not already complete run out on an
+ * ordinary problem: the kernel that gives up records RA_ERR_TIMEOUT, stops its
+ * other roles through a shared flag, lets the copies and products it has in
+ * flight finish (those waits keep their own fixed limit), frees its tensor memory
+ * and returns, and its outputs are undefined. The release build's waits first
+ * block in hardware for a short, system-defined time, so there only waits longer
+ * than that run out. Meant for tests only: an application has no reason to call
+ * it. Limits above the default give RA_ERR_INVALID_ARG. */
 ra_status ring_attn_selftest_wait_limit(uint64_t limit_ns);
 
 /* 1 if this library was built with the kernels' index checks (RA_DEBUG), else 0.

@@ -910,8 +910,12 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
   if (!encode_rows(&tk, k, p.B, p.N, p.G, p.D, p.L, p.X, ml, 32) ||
       !encode_rows(&tv, v, p.B, p.N, p.G, p.D, p.L, p.X, ml, 32))
     return RA_ERR_CUDA;
-  cudaError_t e = launch_decode_partials(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, cs);
+  p.o = o;
+  p.lse = lse;
+  const bool clustered = decode_clustered(p, n_q);
+  cudaError_t e = launch_decode_partials(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, clustered, cs);
   if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (clustered) return RA_OK;
   return launch_result(launch_merge(static_cast<int>(parts), pr->batch, n_q, pr->heads,
                                     pr->head_dim, o_parts, lse_parts, o, p.o_f32 != 0, lse,
                                     cs));

@@ -57,7 +57,10 @@ struct DecSmem {
   static constexpr int kMergeO = 0;
   static constexpr int kMergeM = kWarps * kRows * D * 4;
   static constexpr int kMergeL = kMergeM + kWarps * kRows * 4;
-  static_assert(kMergeL + kWarps * kRows * 4 <= kRing, "merge area inside the ring");
+  // in a cluster, the CTA's own partial for the peers to read: O [row][D], LSE [row]
+  static constexpr int kPartO = kMergeL + kWarps * kRows * 4;
+  static constexpr int kPartL = kPartO + kRows * D * 4;
+  static_assert(kPartL + kRows * 4 <= kRing, "merge area inside the ring");
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -91,8 +94,12 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int col) {
 }
 
 
-// grid: x = g * n_rowgroups + rowgroup, y = segment * n_chunks + chunk, z = batch * P + u
-template <int D>
+// grid: x = g * n_rowgroups + rowgroup, y = segment * n_chunks + chunk, z = batch * P + u.
+// CL: the partials of one (sequence, kv head, row group) are the CTAs of one cluster
+// (cluster dims 1 x segments*chunks x P), which merge them through distributed shared
+// memory and write O and LSE themselves; otherwise each CTA writes its partial to
+// o_parts / lse_parts for the merge kernel.
+template <int D, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_mma_kernel(const __grid_constant__ RingParams p, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, int n_q, int q_pos0, int chunk,
@@ -332,6 +339,13 @@ decode_mma_kernel(const __grid_constant__ RingParams p, const __grid_constant__ 
       Z += f * sm_l[w * kRows + r];
       Y += f * sm_o[(w * kRows + r) * D + col];
     }
+    if constexpr (CL) {
+      // this CTA's normalised partial, in its own shared memory (LSE in log2 units)
+      reinterpret_cast<float*>(smem + L::kPartO)[r * D + col] = Z > 0.f ? Y / Z : 0.f;
+      if (col == 0)
+        reinterpret_cast<float*>(smem + L::kPartL)[r] = Z > 0.f ? M + log2f(Z) : -INFINITY;
+      continue;
+    }
     const int rr = row0 + r, h = g * hpg + rr / n_q, t = rr % n_q;
     // partials [parts, B, n_q, H, d] and [parts, B, H, n_q], parts = P * nseg * n_chunks
     const size_t rows_n = static_cast<size_t>(p.P) * nseg * n_chunks * p.B * n_q * p.H;
@@ -343,30 +357,158 @@ decode_mma_kernel(const __grid_constant__ RingParams p, const __grid_constant__ 
         lse_parts[lo] = Z > 0.f ? (M + log2f(Z)) * kLn2 : -INFINITY;
     }
   }
+  if constexpr (CL) {
+    // Merge of the cluster's partials, the element (row, col) by one thread of the
+    // cluster: LSE = M + log2 sum_c 2^(LSE_c - M), O = sum_c 2^(LSE_c - LSE) O_c,
+    // over the CTAs in rank order (Transformer Math "Ring Attention", "The ring is a
+    // prefill algorithm": one small reduction combines the per-shard partials).
+    cluster_sync();
+    const uint32_t n_cta = cluster_ctas(), rank = cluster_rank();
+    const uint32_t part_o = sbase + L::kPartO, part_l = sbase + L::kPartL;
+    for (int e = static_cast<int>(rank) * kThreads + threadIdx.x; e < n_rows * D;
+         e += static_cast<int>(n_cta) * kThreads) {
+      const int r = e / D, col = e % D;
+      float M = -INFINITY;
+      for (uint32_t c = 0; c < n_cta; ++c)
+        M = fmaxf(M, ld_cluster_f32(map_to_rank(part_l + 4 * r, c)));
+      float Z = 0.f, Y = 0.f;
+      if (M != -INFINITY) {
+        for (uint32_t c = 0; c < n_cta; ++c) {
+          const float lc = ld_cluster_f32(map_to_rank(part_l + 4 * r, c));
+          const float f = (lc == -INFINITY) ? 0.f : ex2(lc - M);
+          Z += f;
+          Y += f * ld_cluster_f32(map_to_rank(part_o + 4 * (r * D + col), c));
+        }
+      }
+      const int rr = row0 + r, h = g * hpg + rr / n_q, t = rr % n_q;
+      const size_t oo = ((static_cast<size_t>(bat) * n_q + t) * p.H + h) * D + col;
+      const size_t q_n = static_cast<size_t>(p.B) * n_q * p.H * D;   // o is [B, n_q, H, d]
+      const float ov = Z > 0.f ? Y / Z : 0.f;
+      if (in_bounds(oo, 1, q_n, p.status)) {
+        if (p.o_f32)
+          static_cast<float*>(p.o)[oo] = ov;
+        else
+          static_cast<__nv_bfloat16*>(p.o)[oo] = __float2bfloat16_rn(ov);
+      }
+      if (col == 0) {
+        const size_t lo = (static_cast<size_t>(bat) * p.H + h) * n_q + t;   // lse [B, H, n_q]
+        if (in_bounds(lo, 1, static_cast<size_t>(p.B) * p.H * n_q, p.status))
+          p.lse[lo] = Z > 0.f ? (M + log2f(Z)) * kLn2 : -INFINITY;
+      }
+    }
+    cluster_sync();   // the peers' partials stay in place until every CTA has read them
+  }
+}
+
+// The cluster merge applies when a row group's partials are at most 8 CTAs (the
+// portable cluster size) and the grid is one wave or less, where the second launch
+// and the partials' round trip through HBM are a visible part of a call's time.
+// (Clusters of 16 CTAs measured slower than the two launches.)
+constexpr int kMaxClusterParts = 8;
+
+template <int D, bool CL>
+cudaError_t set_attrs() {
+  static OncePerContext attr;
+  return attr.run([] {
+    cudaError_t r = cudaFuncSetAttribute(decode_mma_kernel<D, CL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DecSmem<D>::kAlloc);
+    return r;
+  });
+}
+
+struct DecGrid {
+  dim3 grid;
+  int n_rowgroups, n_chunks, chunk, parts;
+};
+
+DecGrid decode_grid(const RingParams& p, int n_q) {
+  DecGrid d;
+  const int rows_total = (p.H / p.G) * n_q;
+  d.n_rowgroups = (rows_total + kRows - 1) / kRows;
+  const int nseg = num_segs(p.layout);
+  const int seg_len = p.S / nseg;
+  d.chunk = decode_chunk_keys(p.S, p.P, p.layout);
+  d.n_chunks = (seg_len + d.chunk - 1) / d.chunk;
+  d.parts = p.P * nseg * d.n_chunks;
+  d.grid = dim3(p.G * d.n_rowgroups, nseg * d.n_chunks, p.B * p.P);
+  return d;
+}
+
+template <int D>
+bool clustered_d(const RingParams& p, int n_q) {
+  const DecGrid d = decode_grid(p, n_q);
+  if (d.parts < 2 || d.parts > kMaxClusterParts) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const long long ctas = static_cast<long long>(d.grid.x) * d.grid.y * d.grid.z;
+  if (ctas > sms) return false;
+  if (set_attrs<D, true>() != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  // whether clusters of this size fit on the device at all (kept per context and size)
+  static std::atomic<unsigned long long> fits_ctx[kMaxClusterParts + 1] = {};
+  static std::atomic<int> fits[kMaxClusterParts + 1] = {};
+  const unsigned long long id = current_context_id();
+  if (id == 0 || fits_ctx[d.parts].load() != id) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = d.grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = DecSmem<D>::kAlloc;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = d.grid.y;
+    at[0].val.clusterDim.z = p.P;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_mma_kernel<D, true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    fits[d.parts].store(n > 0 ? 1 : 0);
+    fits_ctx[d.parts].store(id);
+  }
+  return fits[d.parts].load() != 0;
 }
 
 template <int D>
 cudaError_t launch_d(const RingParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int n_q,
-                     int q_pos0, float* o_parts, float* lse_parts, cudaStream_t st) {
-  const int rows_total = (p.H / p.G) * n_q;
-  const int n_rowgroups = (rows_total + kRows - 1) / kRows;
-  const int nseg = num_segs(p.layout);
-  const int seg_len = p.S / nseg;
-  const int chunk = decode_chunk_keys(p.S, p.P, p.layout);
-  const int n_chunks = (seg_len + chunk - 1) / chunk;
+                     int q_pos0, float* o_parts, float* lse_parts, bool clustered,
+                     cudaStream_t st) {
+  const DecGrid d = decode_grid(p, n_q);
   const int smem = DecSmem<D>::kAlloc;
-  // the shared-memory limit is set once per device context (a decode loop calls this per
-  // token, possibly inside a CUDA graph capture)
-  static OncePerContext attr;
-  const cudaError_t e = attr.run([&] {
-    return cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem);
-  });
+  // the attributes are set once per device context (a decode loop calls this per token,
+  // possibly inside a CUDA graph capture)
+  if (!clustered) {
+    const cudaError_t e = set_attrs<D, false>();
+    if (e != cudaSuccess) return e;
+    decode_mma_kernel<D, false><<<d.grid, kThreads, smem, st>>>(
+        p, tk, tv, n_q, q_pos0, d.chunk, d.n_rowgroups, d.n_chunks, o_parts, lse_parts);
+    return cudaGetLastError();
+  }
+  const cudaError_t e = set_attrs<D, true>();
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.G * n_rowgroups, nseg * n_chunks, p.B * p.P);
-  decode_mma_kernel<D><<<grid, kThreads, smem, st>>>(p, tk, tv, n_q, q_pos0, chunk, n_rowgroups,
-                                                     n_chunks, o_parts, lse_parts);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = d.grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = d.grid.y;
+  at[0].val.clusterDim.z = p.P;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, true>, p, tk, tv, n_q, q_pos0, d.chunk,
+                            d.n_rowgroups, d.n_chunks, o_parts, lse_parts);
 }
 
 }  // namespace
@@ -392,11 +534,15 @@ int decode_parts(int S, int P, int layout) {
   return P * nseg * ((seg_len + chunk - 1) / chunk);
 }
 
+bool decode_clustered(const RingParams& p, int n_q) {
+  return p.D == 64 ? clustered_d<64>(p, n_q) : clustered_d<128>(p, n_q);
+}
+
 cudaError_t launch_decode_partials(const RingParams& p, const CUtensorMap& tk,
                                    const CUtensorMap& tv, int n_q, int q_pos0, float* o_parts,
-                                   float* lse_parts, cudaStream_t st) {
-  return p.D == 64 ? launch_d<64>(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, st)
-                   : launch_d<128>(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, st);
+                                   float* lse_parts, bool clustered, cudaStream_t st) {
+  return p.D == 64 ? launch_d<64>(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, clustered, st)
+                   : launch_d<128>(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, clustered, st);
 }
 
 }  // namespace ra

@@ -160,10 +160,14 @@ cudaError_t launch_selftest_bounds(int* status, cudaStream_t st);
 cudaError_t launch_rows_copy(void* dst, size_t dpitch, const void* src, size_t spitch,
                              size_t width, size_t rows, int blocks, cudaStream_t st);
 // Pass-Q decode, phase 1: per-(shard segment, key chunk) partials into the
-// workspace. tk, tv: [B,N,G,d] views with 32-row boxes.
+// workspace. tk, tv: [B,N,G,d] views with 32-row boxes. With `clustered` (when
+// decode_clustered says so) the partials of a row group are merged inside the
+// launch, through a thread-block cluster, and O and LSE (p.o, p.lse) are written
+// directly: no merge launch follows.
+bool decode_clustered(const RingParams& p, int n_q);
 cudaError_t launch_decode_partials(const RingParams& p, const CUtensorMap& tk,
                                    const CUtensorMap& tv, int n_q, int q_pos0, float* o_parts,
-                                   float* lse_parts, cudaStream_t st);
+                                   float* lse_parts, bool clustered, cudaStream_t st);
 // Keys per chunk of a shard segment in the decode partial phase, and the number
 // of partials (P x segments x chunks per segment).
 int decode_chunk_keys(int S, int P, int layout);

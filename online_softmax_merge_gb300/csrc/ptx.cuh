@@ -69,11 +69,42 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test: true once the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase `parity` of `bar`, for at most limit_ns nanoseconds, and
 // gives up early when *abort (shared memory) becomes non-zero. Returns false on
 // expiry or abort.
+//
+// Release builds poll with try_wait, which may itself block in hardware for a
+// short, system-defined time, and look at the clock and the abort flag every 32
+// polls. Debug builds (RA_DEBUG) poll with the non-blocking test_wait and look at
+// both on every poll, so that a limit of a few nanoseconds (set by the abort-path
+// tests) makes any wait that is not already complete run out; there a limit under
+// 1000 ns is a number of polls.
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                              const volatile int* abort) {
+#ifdef RA_DEBUG
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint64_t polls = 1;; ++polls) {
+    if (mbar_test(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    // %globaltimer may advance in steps of up to a microsecond; a limit below that
+    // counts polls instead
+    if (limit_ns < 1000 ? polls >= limit_ns : global_ns() - t0 > limit_ns) return false;
+  }
+#else
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
@@ -83,6 +114,39 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, uint
     if (abort != nullptr && *abort) return false;
     if (global_ns() - t0 > limit_ns) return false;
   }
+#endif
+}
+
+// ----------------------------------------------------------------------------
+// Thread-block clusters: rank, barrier, and loads from a peer CTA's shared memory.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctas() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+// Every thread of every CTA of the cluster arrives (release) and waits (acquire):
+// shared-memory writes before it are visible to the cluster's loads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of the same shared-memory location in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // ----------------------------------------------------------------------------

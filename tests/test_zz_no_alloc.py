@@ -31,7 +31,9 @@ def _p(t):
 def test_noalloc_decode_equals_decode_on_calls_in_a_row():
     lib = ra.load()
     dev = torch.device("cuda:0")
-    w = Workload("noalloc", 2, 16 * 1024, 8, 2, 128, 4, "contiguous", True, seed=41)
+    # 32 shards: more partials per row group than one thread-block cluster merges, so
+    # the partials go through the scratch and the merge kernel
+    w = Workload("noalloc", 2, 64 * 1024, 8, 2, 128, 32, "contiguous", True, seed=41)
     _, k, v = (t.to(dev) for t in make_qkv(w))
     pr = ra.problem(w.batch, w.seqlen, w.heads, w.kv_heads, w.head_dim, w.P, True, w.layout)
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
@@ -39,7 +41,7 @@ def test_noalloc_decode_equals_decode_on_calls_in_a_row():
     small = lib.ring_attn_decode_workspace_bytes(ctypes.byref(pr), 1)
     assert small < big <= _lib.RA_DECODE_SCRATCH_BYTES
     # (n_q, first query position, seed): large, then small, then large again
-    calls = ((16, 9000, 1), (1, w.seqlen - 1, 2), (16, w.seqlen - 16, 3))
+    calls = ((16, 40000, 1), (1, w.seqlen - 1, 2), (16, w.seqlen - 16, 3))
     for n_q, q_pos0, seed in calls:
         g = torch.Generator(device=dev).manual_seed(seed)
         q = torch.randn((w.batch, n_q, w.heads, w.head_dim), generator=g,
