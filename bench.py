@@ -446,7 +446,7 @@ def run_ours(args, w):
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     mean_launch_s = statistics.mean(launch_ms) * 1e-3
     achieved = flops_step / mean_launch_s / 1e12
-    traffic = load_traffic(f"ring_tc_kernel:{w.name}")
+    traffic = load_traffic(f"ring_tc_kernel:{w.name}:{args.out_dtype}")
 
     # ---- the same forward writing O in the other element type (bf16 <-> fp32)
     other = None
