@@ -137,7 +137,8 @@ typedef struct {
 
 /* Full ring forward: every virtual device u folds all P shards in ring order
  * b = (u - s) mod P, s = 0..P-1, and writes O = y / z (bf16, round to nearest
- * even) and LSE = m + ln z (fp32). Tiles that the causal mask leaves empty are
+ * even, or fp32 with p->o_dtype = RA_DTYPE_F32) and LSE = m + ln z (fp32). The
+ * bf16 output is exactly the fp32 one rounded. Tiles that the causal mask leaves empty are
  * skipped. Source: "Ring Attention" (aarnphm.xyz), recurrence display and
  * O = y/z; "Part 4: Ring Attention" §4.3 and §4.8.1.
  * q, k, v in; o, lse out (device). Errors: see conventions. */
@@ -217,7 +218,8 @@ ra_status ring_attn_step_simt(const ra_problem* p, int32_t s, int32_t first,
                               const void* q, const void* k, const void* v,
                               float* m, float* z, float* y, void* stream);
 
-/* Running state -> result: O = y / z (bf16), LSE = m + ln z (fp32); z = 0 gives
+/* Running state -> result: O = y / z (bf16, or fp32 with p->o_dtype =
+ * RA_DTYPE_F32), LSE = m + ln z (fp32); z = 0 gives
  * O = 0, LSE = -inf. Source: "Ring Attention" (aarnphm.xyz), O = y/z; "Part 4"
  * §4.4 FINAL. m, z, y in; o, lse out (device). */
 ra_status ring_attn_finalize(const ra_problem* p, const float* m, const float* z,
@@ -243,14 +245,18 @@ ra_status ring_attn_merge(int32_t n_parts, int32_t batch, int32_t seqlen, int32_
  * device u scores all queries against its own shard only and writes a
  * normalised partial (O_u, LSE_u) into the workspace (a shard is cut into key
  * chunks, each one more partial). Phase 2: the partials are combined by the
- * ring_attn_merge kernel. Under the causal mask a query sees key positions
+ * ring_attn_merge kernel. When a row group's partials come from at most 8 CTAs
+ * and the grid is one wave or less, those CTAs run as one thread-block cluster
+ * and combine the partials through distributed shared memory instead: one launch,
+ * and the workspace is not touched. Under the causal mask a query sees key positions
  * <= its own. Source: Transformer Math "Ring Attention" (aicassindra), "The ring
  * is a prefill algorithm" (broadcast the query, partial per shard, one
  * reduction); "Part 4: Ring Attention" (Fofadiya) §4.9.4.4 (pass-Q).
  * q [B, n_q, H, d] bf16, k, v [B, N, G, d] bf16 in; o [B, n_q, H, d] bf16 and
- * lse [B, H, n_q] fp32 out. workspace: caller-owned device memory of at least
- * ring_attn_decode_workspace_bytes(p, n_q) bytes, 16-byte aligned, overwritten.
- * 1 <= n_q <= 4096; with causal = 1, q_pos0 + n_q <= N. Two launches on stream. */
+ * lse [B, H, n_q] fp32 out (o fp32 with p->o_dtype = RA_DTYPE_F32). workspace:
+ * caller-owned device memory of at least ring_attn_decode_workspace_bytes(p, n_q)
+ * bytes, 16-byte aligned, overwritten. 1 <= n_q <= 4096; with causal = 1,
+ * q_pos0 + n_q <= N. One or two launches on stream. */
 ra_status ring_attn_decode(const ra_problem* p, int32_t n_q, int32_t q_pos0, const void* q,
                            const void* k, const void* v, void* o, float* lse, void* workspace,
                            size_t workspace_bytes, void* stream);
@@ -301,7 +307,8 @@ ra_status ring_attn_decode_noalloc(const ra_problem* p, int32_t n_q, int32_t q_p
  * LSE = -inf contributes nothing. Probabilities and dS are rounded to bf16 for
  * the tensor-core products; accumulation is fp32; dq, dk, dv are written as
  * bf16 (round to nearest even), every element overwritten.
- * q, o, dout [B, N, H, d] bf16, k, v [B, N, G, d] bf16, lse [B, H, N] fp32 in;
+ * q, dout [B, N, H, d] bf16, o [B, N, H, d] bf16 (fp32 with p->o_dtype =
+ * RA_DTYPE_F32), k, v [B, N, G, d] bf16, lse [B, H, N] fp32 in;
  * dq [B, N, H, d], dk, dv [B, N, G, d] bf16 out (device). workspace:
  * caller-owned device memory of at least ring_attn_bwd_workspace_bytes(p)
  * bytes, 16-byte aligned, overwritten. Three launches on stream. */

@@ -75,26 +75,42 @@ def test_backward_graph_replays_bit_exact():
         assert torch.equal(a, b)
 
 
-def test_decode_graph_replays_bit_exact():
-    _, k, v = (t.to(DEV) for t in make_qkv(W))
+# P = 4: four partials per row group, merged inside a thread-block cluster (one launch);
+# P = 16: sixteen partials, through the workspace and the merge kernel (two launches)
+@pytest.mark.parametrize("P", [4, 16])
+def test_decode_graph_replays_bit_exact(P):
+    w = W.with_(P=P)                              # 1184 tokens: 296 per shard at P = 4, 74 at 16
+    _, k, v = (t.to(DEV) for t in make_qkv(w))
     n_q = 2
     gen = torch.Generator(device="cpu").manual_seed(702)
-    qd = torch.randn((W.batch, n_q, W.heads, W.head_dim), generator=gen).to(torch.bfloat16).to(DEV)
-    need = ra.decode_workspace_bytes(W.batch, W.seqlen, W.heads, W.kv_heads, W.head_dim, W.P,
-                                     n_q, W.layout, W.causal)
+    qd = torch.randn((w.batch, n_q, w.heads, w.head_dim), generator=gen).to(torch.bfloat16).to(DEV)
+    need = ra.decode_workspace_bytes(w.batch, w.seqlen, w.heads, w.kv_heads, w.head_dim, w.P,
+                                     n_q, w.layout, w.causal)
     ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=DEV)
     o = torch.empty_like(qd)
-    lse = torch.empty((W.batch, W.heads, n_q), dtype=torch.float32, device=DEV)
-    pos = W.seqlen - n_q
-    g = capture(lambda: ra.decode(qd, k, v, W.P, pos, W.layout, W.causal, workspace=ws, out=o,
+    lse = torch.empty((w.batch, w.heads, n_q), dtype=torch.float32, device=DEV)
+    pos = w.seqlen - n_q
+    g = capture(lambda: ra.decode(qd, k, v, w.P, pos, w.layout, w.causal, workspace=ws, out=o,
                                   lse=lse))
     for step in range(2):
         if step:                                  # the next token's query
             qd.copy_(torch.randn(qd.shape, generator=gen).to(torch.bfloat16))
         got = replay(g, [o, lse])
-        ref = ra.decode(qd, k, v, W.P, pos, W.layout, W.causal)
+        ref = ra.decode(qd, k, v, w.P, pos, w.layout, w.causal)
         torch.cuda.synchronize(DEV)
         assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+
+
+def test_fp32_output_forward_graph_replays_bit_exact():
+    q, k, v = (t.to(DEV) for t in make_qkv(W))
+    o = torch.empty(q.shape, dtype=torch.float32, device=DEV)
+    lse = torch.empty((W.batch, W.heads, W.seqlen), dtype=torch.float32, device=DEV)
+    g = capture(lambda: ra.fwd(q, k, v, W.P, W.layout, W.causal, out=o, lse=lse,
+                               out_dtype=torch.float32))
+    got = replay(g, [o, lse])
+    ref = ra.fwd(q, k, v, W.P, W.layout, W.causal, out_dtype=torch.float32)
+    torch.cuda.synchronize(DEV)
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
 
 
 def test_merge_and_step_path_graphs_replay_bit_exact():
