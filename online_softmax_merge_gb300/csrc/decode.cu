@@ -422,31 +422,57 @@ struct DecGrid {
   int n_rowgroups, n_chunks, chunk, parts;
 };
 
-DecGrid decode_grid(const RingParams& p, int n_q) {
+DecGrid decode_grid(const RingParams& p, int n_q, int chunk) {
   DecGrid d;
   const int rows_total = (p.H / p.G) * n_q;
   d.n_rowgroups = (rows_total + kRows - 1) / kRows;
   const int nseg = num_segs(p.layout);
   const int seg_len = p.S / nseg;
-  d.chunk = decode_chunk_keys(p.S, p.P, p.layout);
+  d.chunk = chunk;
   d.n_chunks = (seg_len + d.chunk - 1) / d.chunk;
   d.parts = p.P * nseg * d.n_chunks;
   d.grid = dim3(p.G * d.n_rowgroups, nseg * d.n_chunks, p.B * p.P);
   return d;
 }
 
-template <int D>
-bool clustered_d(const RingParams& p, int n_q) {
-  const DecGrid d = decode_grid(p, n_q);
-  if (d.parts < 2 || d.parts > kMaxClusterParts) return false;
+long long ctas_of(const DecGrid& d) {
+  return static_cast<long long>(d.grid.x) * d.grid.y * d.grid.z;
+}
+
+// Keys per chunk of the one-launch form: the chunking of the two-launch form (which
+// sizes the workspace), halved while the row group's partials stay within one
+// cluster, the grid within one wave and the chunks at 256 keys or more. The
+// one-launch form never touches the workspace, so its chunks may be finer; a
+// small-P decode then runs on more CTAs, each streaming fewer keys.
+int cluster_chunk(const RingParams& p, int n_q, int sms) {
+  int chunk = decode_chunk_keys(p.S, p.P, p.layout);
+  for (;;) {
+    const int half = ((chunk / 2) + kTileKeys - 1) / kTileKeys * kTileKeys;
+    if (half < 256 || half >= chunk) break;
+    const DecGrid d = decode_grid(p, n_q, half);
+    if (d.parts > kMaxClusterParts || ctas_of(d) > sms) break;
+    chunk = half;
+  }
+  return chunk;
+}
+
+int device_sms() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     (void)cudaGetLastError();
-    return false;
+    return 0;
   }
-  const long long ctas = static_cast<long long>(d.grid.x) * d.grid.y * d.grid.z;
-  if (ctas > sms) return false;
+  return sms;
+}
+
+template <int D>
+bool clustered_d(const RingParams& p, int n_q) {
+  const int sms = device_sms();
+  if (sms <= 0) return false;
+  const DecGrid d = decode_grid(p, n_q, cluster_chunk(p, n_q, sms));
+  if (d.parts < 2 || d.parts > kMaxClusterParts) return false;
+  if (ctas_of(d) > sms) return false;
   if (set_attrs<D, true>() != cudaSuccess) {
     (void)cudaGetLastError();
     return false;
@@ -482,7 +508,9 @@ template <int D>
 cudaError_t launch_d(const RingParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int n_q,
                      int q_pos0, float* o_parts, float* lse_parts, bool clustered,
                      cudaStream_t st) {
-  const DecGrid d = decode_grid(p, n_q);
+  const DecGrid d = decode_grid(
+      p, n_q,
+      clustered ? cluster_chunk(p, n_q, device_sms()) : decode_chunk_keys(p.S, p.P, p.layout));
   const int smem = DecSmem<D>::kAlloc;
   // the attributes are set once per device context (a decode loop calls this per token,
   // possibly inside a CUDA graph capture)
