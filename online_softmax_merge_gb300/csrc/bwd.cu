@@ -78,11 +78,13 @@ template <int D>
 struct BwdSmem {
   static constexpr int kChunk = 128 * 128;          // 128 rows x 64 bf16 (128 B, swizzled)
   static constexpr int kTile = (D / 64) * kChunk;   // one [128 x D] bf16 tile
+  // stages of the streamed Q and dO tiles: three where shared memory allows (d = 64)
+  static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kFix = 0;                    // two stationary tiles
-  static constexpr int kStage = 2 * kTile;          // two stages of two streamed tiles
-  static constexpr int kAext = 6 * kTile;           // dK/dV kernel: key-side extension (ones)
+  static constexpr int kStage = 2 * kTile;          // kStages stages of two streamed tiles
+  static constexpr int kAext = (2 + 2 * kStages) * kTile;   // key-side extension (ones)
   static constexpr int kExt = kAext + kExtBytes;    // + stage: query-side extensions of Q, dO
-  static constexpr int kBar = kExt + 2 * 2 * kExtBytes;
+  static constexpr int kBar = kExt + kStages * 2 * kExtBytes;
   static constexpr int kBytes = kBar + 256;
   // One CTA per SM: it owns all 512 TMEM columns.
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -100,24 +102,26 @@ struct DqSmem {
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
-// dK/dV kernel barriers. A stage's Q and dO tiles are tracked apart: dO(t) is
-// last read by dV(t), which runs before dK(t), Q's last reader, so dO(t + 2) can
-// start loading before the stage's Q slot is free.
-enum : int {
-  kBarFix = 0,      // stationary tiles landed
-  kBarFull = 1,     // + stage: Q tile and its extension landed
-  kBarEmpty = 3,    // + stage: dK done with the stage's Q
-  kBarSF = 5,       // score tile in TMEM
-  kBarDPF = 6,      // dP tile in TMEM
-  kBarW1 = 7,       // workers: phase 1 done (8 arrivals)
-  kBarW2 = 8,       // workers: dS written (8 arrivals)
-  kBarDone = 9,     // every MMA of the CTA completed
-  kBarDrain = 10,
-  kBarFullO = 11,   // + stage: dO tile and its extension landed
-  kBarEmptyO = 13,  // + stage: dV done with the stage's dO
-  kNumBars = 15
+// dK/dV kernel barriers, for NS stages of streamed tiles. A stage's Q and dO tiles
+// are tracked apart: dO(t) is last read by dV(t), which runs before dK(t), Q's last
+// reader, so dO(t + NS) can start loading before the stage's Q slot is free.
+constexpr int kBarFix = 0;   // stationary tiles landed (both backward kernels)
+template <int NS>
+struct BwdBars {
+  static constexpr int kFull = 1;               // + stage: Q tile and its extension landed
+  static constexpr int kEmpty = 1 + NS;         // + stage: dK done with the stage's Q
+  static constexpr int kSF = 1 + 2 * NS;        // score tile in TMEM (score buffer 0)
+  static constexpr int kDPF = kSF + 1;          // dP tile in TMEM
+  static constexpr int kW1 = kSF + 2;           // workers: phase 1 done (8 arrivals)
+  static constexpr int kW2 = kSF + 3;           // workers: dS written (8 arrivals)
+  static constexpr int kDone = kSF + 4;         // every MMA of the CTA completed
+  static constexpr int kDrain = kSF + 5;
+  static constexpr int kFullO = kSF + 6;        // + stage: dO tile and its extension landed
+  static constexpr int kEmptyO = kFullO + NS;   // + stage: dV done with the stage's dO
+  static constexpr int kSF1 = kEmptyO + NS;     // d = 64: score tile in score buffer 1
+  static constexpr int kNum = kSF1 + 1;
+  static_assert(8 * kNum + 8 <= 256, "barrier area");
 };
-static_assert(8 * kNumBars + 8 <= 256, "barrier area");
 
 __device__ __forceinline__ void record_failure(const BwdParams& p, volatile int* abort_flag) {
   atomicCAS(p.status, 0, static_cast<int>(RA_ERR_TIMEOUT));
@@ -391,6 +395,12 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
                 const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap text) {
   using L = BwdSmem<D>;
+  constexpr int NS = L::kStages;
+  using Bars = BwdBars<NS>;
+  constexpr int kBarFull = Bars::kFull, kBarEmpty = Bars::kEmpty, kBarSF = Bars::kSF,
+                kBarDPF = Bars::kDPF, kBarW1 = Bars::kW1, kBarW2 = Bars::kW2,
+                kBarDone = Bars::kDone, kBarDrain = Bars::kDrain, kBarFullO = Bars::kFullO,
+                kBarEmptyO = Bars::kEmptyO, kBarSF1 = Bars::kSF1, kNumBars = Bars::kNum;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -444,12 +454,17 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  constexpr uint32_t kColDK = 0, kColDV = D, kColS = 256, kColDP = 384;
+  // TMEM: dK, dV (fp32), the score tile S^T and dP^T (fp32, overwritten by A^T and dS^T
+  // as bf16). At d = 64 the free columns [128, 256) hold a second score buffer: tile t's
+  // scores go to buffer t % 2, so the next tile's scores need not wait for dV to have
+  // read this tile's A^T.
+  constexpr bool kTwoS = (D == 64);
+  constexpr uint32_t kColDK = 0, kColDV = D, kColS = 256, kColS1 = 128, kColDP = 384;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
-      uint32_t nfq[2] = {}, nfo[2] = {};   // loads issued per barrier (for the drain on abort)
+      uint32_t nfq[NS] = {}, nfo[NS] = {};   // loads issued per barrier (for the drain on abort)
       bool ok = true;
       mbar_arrive_expect_tx(bar(kBarFix), 2 * L::kTile + kExtBytes);
 #pragma unroll
@@ -461,13 +476,13 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
       }
       tma_load_2d(sbase + L::kAext, &text, bar(kBarFix), 0, 2 * p.tiles * 128);
       walk_qtiles<ZIG>(p, w, [&](int t, int h, const Seg& sq, int qt) {
-        const int st = t & 1;
-        const uint32_t n = static_cast<uint32_t>(t >> 1);
+        const int st = t % NS;
+        const uint32_t n = static_cast<uint32_t>(t / NS);
         const uint32_t dst = sbase + L::kStage + st * 2 * L::kTile;
         const int tile = ((w.bat * p.H + h) * p.X + sq.chunk) * p.nt + qt;
         const uint32_t ext = sbase + L::kExt + st * 2 * kExtBytes;
-        // dO(t) and its extension (-D), once dV(t - 2) has read the slot
-        if (t >= 2 && !bounded_wait(bar(kBarEmptyO + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+        // dO(t) and its extension (-D), once dV(t - NS) has read the slot
+        if (t >= NS && !bounded_wait(bar(kBarEmptyO + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           return false;
         }
@@ -478,9 +493,9 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
                    sq.chunk, qt * 128, w.bat);
         tma_load_2d(ext + kExtBytes, &text, bar(kBarFullO + st), 0, (p.tiles + tile) * 128);
 #pragma unroll
-        for (int x = 0; x < 2; ++x) nfo[x] += (x == st);
-        // Q(t) and its extension (-LSE/scale), once dK(t - 2) has read the slot
-        if (t >= 2 && !bounded_wait(bar(kBarEmpty + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
+        for (int x = 0; x < NS; ++x) nfo[x] += (x == st);
+        // Q(t) and its extension (-LSE/scale), once dK(t - NS) has read the slot
+        if (t >= NS && !bounded_wait(bar(kBarEmpty + st), (n - 1) & 1, p.timeout_ns, abort_flag)) {
           ok = false;
           return false;
         }
@@ -491,14 +506,14 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
                    qt * 128, w.bat);
         tma_load_2d(ext, &text, bar(kBarFull + st), 0, tile * 128);
 #pragma unroll
-        for (int x = 0; x < 2; ++x) nfq[x] += (x == st);
+        for (int x = 0; x < NS; ++x) nfq[x] += (x == st);
         return true;
       });
       if (!ok) {
         record_failure(p, abort_flag);
         bounded_wait(bar(kBarFix), 0, kDrainNs, nullptr);
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
+        for (int x = 0; x < NS; ++x) {
           if (nfq[x]) bounded_wait(bar(kBarFull + x), (nfq[x] - 1) & 1, kDrainNs, nullptr);
           if (nfo[x]) bounded_wait(bar(kBarFullO + x), (nfo[x] - 1) & 1, kDrainNs, nullptr);
         }
@@ -519,8 +534,11 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     // S^T (which = 0) or dP^T (which = 1) of stage st, with its extension slice
     const uint64_t dA = smem_desc_sw32(sbase + L::kAext);
     constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, false);
-    auto products = [&](int st, int which) {
-      const uint32_t d_tmem = which == 0 ? tmem + kColS : tmem + kColDP;
+    // score buffer of tile t
+    auto sbuf = [&](int t) -> uint32_t { return (kTwoS && (t & 1)) ? kColS1 : kColS; };
+    auto sfbar = [&](int t) -> int { return (kTwoS && (t & 1)) ? kBarSF1 : kBarSF; };
+    auto products = [&](int st, int which, int t) {
+      const uint32_t d_tmem = which == 0 ? tmem + sbuf(t) : tmem + kColDP;
       issue_ss<D>(d_tmem, which == 0 ? dK : dV, sdesc(st, which, false));
       mma_ss(d_tmem, dA, smem_desc_sw32(sbase + L::kExt + st * 2 * kExtBytes + which * kExtBytes),
              kIdesc, 1u);
@@ -530,7 +548,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     if (ok) {
       tc_fence_after_sync();
       if (elect_one()) {
-        products(0, 0);     // S^T(0) = K Q^T - LSE/scale
+        products(0, 0, 0);  // S^T(0) = K Q^T - LSE/scale
         mma_commit(bar(kBarSF));
       }
       __syncwarp();
@@ -539,37 +557,47 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     if (ok) {
       tc_fence_after_sync();
       if (elect_one()) {
-        products(0, 1);     // dP^T(0) = V dO^T - D
+        products(0, 1, 0);  // dP^T(0) = V dO^T - D
         mma_commit(bar(kBarDPF));
       }
       __syncwarp();
     }
+    // Order per tile t: dV(t) | S^T(t+1) | dK(t) | dP^T(t+1). With two score buffers
+    // (d = 64) S^T(t+1) goes first: its buffer last held A^T(t-1), which dV(t-1) read
+    // before it in the same order of MMAs, and the workers were done with it at W1(t-1).
     for (int t = 0; t < T && ok; ++t) {
-      const int st = t & 1, st1 = (t + 1) & 1;
-      const uint32_t ph1 = static_cast<uint32_t>((t + 1) >> 1) & 1;
+      const int st = t % NS, st1 = (t + 1) % NS;
+      const uint32_t ph1 = static_cast<uint32_t>((t + 1) / NS) & 1;
       const bool has_next = t + 1 < T;
       const uint32_t par = static_cast<uint32_t>(t) & 1;
+      auto next_scores = [&]() -> bool {
+        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarFull + st1), ph1, p.timeout_ns, abort_flag)))
+          return false;
+        tc_fence_after_sync();
+        if (elect_one()) {
+          products(st1, 0, t + 1);
+          mma_commit(bar(sfbar(t + 1)));
+        }
+        __syncwarp();
+        return true;
+      };
+      if (kTwoS && has_next && !next_scores()) {
+        ok = false;
+        break;
+      }
       if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW1), par, p.timeout_ns, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       if (elect_one()) {
-        issue_ts<D>(tDV, tS, sdesc(st, 1, true), t > 0);   // dV += A^T dO
+        issue_ts<D>(tDV, tmem + sbuf(t), sdesc(st, 1, true), t > 0);   // dV += A^T dO
         mma_commit(bar(kBarEmptyO + st));
       }
       __syncwarp();
-      if (has_next) {
-        if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarFull + st1), ph1, p.timeout_ns, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        if (elect_one()) {
-          products(st1, 0);
-          mma_commit(bar(kBarSF));
-        }
-        __syncwarp();
+      if (!kTwoS && has_next && !next_scores()) {
+        ok = false;
+        break;
       }
       if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarW2), par, p.timeout_ns, abort_flag))) {
         ok = false;
@@ -589,7 +617,7 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
         }
         tc_fence_after_sync();
         if (elect_one()) {
-          products(st1, 1);
+          products(st1, 1, t + 1);
           mma_commit(bar(kBarDPF));
         }
         __syncwarp();
@@ -610,7 +638,8 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     const bool valid = j < w.sk.len;
     const int kpos = w.sk.base + j * w.sk.stride;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + kColS + lane_off + half * 64;
+    const uint32_t tS0 = tmem + kColS + lane_off + half * 64;
+    const uint32_t tS1 = tmem + kColS1 + lane_off + half * 64;
     const uint32_t tDP = tmem + kColDP + lane_off + half * 64;
     const float2 cc = make_float2(p.scale_log2, p.scale_log2);
     // First local query row of the current query segment that sees this key (kept per
@@ -620,8 +649,13 @@ bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUt
     walk_qtiles<ZIG>(p, w, [&](int t, int, const Seg& sq, int qt) {
       const uint32_t par = static_cast<uint32_t>(t) & 1;
       // phase 1: A^T = exp2((S^T - LSE/scale) * scale * log2e), masked; the
-      // products already subtracted LSE/scale
-      if (!__all_sync(0xffffffffu, bounded_wait(bar(kBarSF), par, p.timeout_ns, abort_flag))) {
+      // products already subtracted LSE/scale. Score buffer t % 2 at d = 64 (each
+      // buffer completes once every two tiles), the one buffer otherwise.
+      const bool b1 = kTwoS && (t & 1);
+      const uint32_t tS = b1 ? tS1 : tS0;
+      const uint32_t spar = kTwoS ? (static_cast<uint32_t>(t) >> 1) & 1 : par;
+      if (!__all_sync(0xffffffffu,
+                      bounded_wait(bar(b1 ? kBarSF1 : kBarSF), spar, p.timeout_ns, abort_flag))) {
         ok = false;
         return false;
       }
@@ -802,7 +836,8 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
   const uint32_t sbase = smem_u32(smem);
   // barriers: kBarFix, then NS full, NS empty, and the per-step ones after them
   constexpr int kFull = 1, kEmpty = 1 + NS, kSF = 1 + 2 * NS, kDPF = kSF + 1, kW1 = kSF + 2,
-                kW2 = kSF + 3, kDone = kSF + 4, kDrain = kSF + 5, kBars = kSF + 6;
+                kW2 = kSF + 3, kDone = kSF + 4, kDrain = kSF + 5, kSF1 = kSF + 6,
+                kBars = kSF + 7;
   static_assert(8 * kBars + 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBar + 8 * kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBar + 8 * kBars + 4);
@@ -850,8 +885,13 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   // TMEM: S, dP (fp32), dQ (fp32), and the stationary Q and dO tiles as bf16
-  // pairs, the A operands of S = Q K^T and dP = dO V^T.
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 384, kColDO = 384 + D / 2;
+  // pairs, the A operands of S = Q K^T and dP = dO V^T. At d = 64 a second score
+  // buffer fits: tile t's scores go to buffer t % 2, so the next tile's scores need
+  // not wait for the workers to have read this tile's.
+  constexpr bool kTwoS = (D == 64);
+  constexpr uint32_t kColS = 0, kColS1 = 128, kColDP = kTwoS ? 256 : 128,
+                     kColDQ = kColDP + 128, kColQ = kColDQ + D, kColDO = kColQ + D / 2;
+  static_assert(kColDO + D / 2 <= kTmemCols, "TMEM columns");
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA
@@ -903,7 +943,7 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
     if (ok) {
       tc_fence_after_sync();
       if (elect_one()) {
-        issue_ts_kmajor<D>(tS, tQ, kdesc(0, false));    // S(0) = Q K^T
+        issue_ts_kmajor<D>(tS, tQ, kdesc(0, false));    // S(0) = Q K^T, score buffer 0
         mma_commit(bar(kSF));
         issue_ts_kmajor<D>(tDP, tDO, vdesc(0));        // dP(0) = dO V^T
         mma_commit(bar(kDPF));
@@ -916,16 +956,21 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
       const bool has_next = t + 1 < T;
       const uint32_t par = static_cast<uint32_t>(t) & 1;
       if (has_next) {
-        // the workers have read S(t): S(t+1) may overwrite it
-        if (!__all_sync(0xffffffffu, bounded_wait(bar(kW1), par, p.timeout_ns, abort_flag) &&
-                                     bounded_wait(bar(kFull + st1), ph1, p.timeout_ns, abort_flag))) {
+        // One score buffer: the workers have read S(t), so S(t+1) may overwrite it. Two
+        // (d = 64): S(t+1) goes to the buffer of S(t-1), which the workers finished
+        // reading before they wrote dS(t-1), and that was waited for (W2) before dQ(t-1).
+        const bool ready = kTwoS ? bounded_wait(bar(kFull + st1), ph1, p.timeout_ns, abort_flag)
+                                 : bounded_wait(bar(kW1), par, p.timeout_ns, abort_flag) &&
+                                       bounded_wait(bar(kFull + st1), ph1, p.timeout_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, ready)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         if (elect_one()) {
-          issue_ts_kmajor<D>(tS, tQ, kdesc(st1, false));
-          mma_commit(bar(kSF));
+          const bool b1 = kTwoS && ((t + 1) & 1);
+          issue_ts_kmajor<D>(b1 ? tmem + kColS1 : tS, tQ, kdesc(st1, false));
+          mma_commit(bar(b1 ? kSF1 : kSF));
         }
         __syncwarp();
       }
@@ -961,7 +1006,8 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
     const bool valid = i < w.sq.len;
     const int qpos = valid ? w.sq.base + i * w.sq.stride : -1;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + kColS + lane_off + half * 64;
+    const uint32_t tS0 = tmem + kColS + lane_off + half * 64;
+    const uint32_t tS1 = tmem + kColS1 + lane_off + half * 64;
     const uint32_t tDP = tmem + kColDP + lane_off + half * 64;
     const float* st_row = stats_tile(p, w.bat, w.h, w.sq.chunk, w.qt) + quarter * 32 + lane;
     const bool st_ok = in_bounds(static_cast<size_t>(st_row - p.ws), 129, stats_elems(p), p.status);
@@ -1008,7 +1054,11 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
         seg_key = sk.base;
         row_vis = seg_visible(sk, p.causal, 0, sk.len, qpos);
       }
-      if (!__all_sync(0xffffffffu, bounded_wait(bar(kSF), par, p.timeout_ns, abort_flag))) {
+      // score buffer t % 2 at d = 64 (each completes once every two tiles)
+      const bool b1 = kTwoS && (t & 1);
+      const uint32_t spar = kTwoS ? (static_cast<uint32_t>(t) >> 1) & 1 : par;
+      if (!__all_sync(0xffffffffu,
+                      bounded_wait(bar(b1 ? kSF1 : kSF), spar, p.timeout_ns, abort_flag))) {
         ok = false;
         return false;
       }
@@ -1016,7 +1066,7 @@ bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUten
       float a[64];
       {
         uint32_t r[64];
-        tmem_ld_x64(tS, r);
+        tmem_ld_x64(b1 ? tS1 : tS0, r);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           const float2 x = ffma2(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), cc, ml);
