@@ -393,6 +393,14 @@ ra_status ring_attn_selftest_bounds(void* stream);
 /* Human-readable name of a status code (static string). */
 const char* ra_status_str(ra_status s);
 
+/* The cudaError_t behind the most recent RA_ERR_CUDA that a call of this library
+ * returned on the calling host thread (0 before any). A tensor map the driver
+ * refused to encode reads cudaErrorInvalidValue. Pure host code. */
+int32_t ring_attn_last_cuda_error(void);
+
+/* CUDA's name for a cudaError_t value (cudaGetErrorName; a static string). */
+const char* ring_attn_cuda_error_name(int32_t code);
+
 /* Library ABI version (major*100 + minor). */
 int32_t ring_attn_version(void);
 

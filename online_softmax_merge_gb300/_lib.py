@@ -58,6 +58,8 @@ SIGNATURES = {
     "ring_attn_selftest_bounds": (_i32, [_vp]),
     "ring_attn_debug_checks": (_i32, []),
     "ra_status_str": (ctypes.c_char_p, [_i32]),
+    "ring_attn_last_cuda_error": (_i32, []),
+    "ring_attn_cuda_error_name": (ctypes.c_char_p, [_i32]),
     "ring_attn_version": (_i32, []),
 }
 
@@ -65,10 +67,14 @@ _LIB = None
 
 
 class RingAttnError(RuntimeError):
-    def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn} returned {STATUS_NAMES.get(code, code)}")
+    def __init__(self, fn: str, code: int, cuda_error: int = 0, cuda_name: str = ""):
+        what = f"{fn} returned {STATUS_NAMES.get(code, code)}"
+        if cuda_error:
+            what += f" ({cuda_name or 'cudaError'} = {cuda_error})"
+        super().__init__(what)
         self.fn = fn
         self.code = code
+        self.cuda_error = cuda_error
 
 
 def load() -> ctypes.CDLL:
@@ -91,4 +97,8 @@ def load() -> ctypes.CDLL:
 
 def check(fn: str, code: int) -> None:
     if code != RA_OK:
-        raise RingAttnError(fn, code)
+        cuda_error, name = 0, ""
+        if code == RA_ERR_CUDA and _LIB is not None:
+            cuda_error = int(_LIB.ring_attn_last_cuda_error())
+            name = (_LIB.ring_attn_cuda_error_name(cuda_error) or b"").decode()
+        raise RingAttnError(fn, code, cuda_error, name)

@@ -49,6 +49,14 @@ unsigned long long current_context_id() {
 
 namespace {
 
+// The CUDA error behind the calling thread's most recent RA_ERR_CUDA (0 before any);
+// cuda_failed records it and returns RA_ERR_CUDA.
+thread_local int32_t g_last_cuda_error = 0;
+ra_status cuda_failed(cudaError_t e) {
+  g_last_cuda_error = static_cast<int32_t>(e);
+  return RA_ERR_CUDA;
+}
+
 // Status word of the GPU: a kernel that gives up on a wait records its code here.
 __device__ int g_status = 0;
 
@@ -73,7 +81,8 @@ DevInfo g_dev[kMaxDevices];
 // (the status word's device address belongs to a context).
 ra_status current_device(DevInfo** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_failed(e);
   if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
   const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lk(g_mu);
@@ -81,17 +90,17 @@ ra_status current_device(DevInfo** out) {
   if (!d.init || id == 0 || d.ctx != id) {
     d.init = false;
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return RA_ERR_CUDA;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_failed(e);
     d.sm103 = (major == 10 && minor == 3);
     d.ordinal = dev;
     d.status = nullptr;
     if (d.sm103) {
       void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) {
+      if ((e = cudaGetSymbolAddress(&ptr, g_status)) != cudaSuccess) {
         (void)cudaGetLastError();
-        return RA_ERR_CUDA;
+        return cuda_failed(e);
       }
       d.status = static_cast<int*>(ptr);
     }
@@ -294,7 +303,7 @@ bool encode_rows(CUtensorMap* m, const void* base, int B, int N, int heads, int 
   return r == CUDA_SUCCESS;
 }
 
-ra_status launch_result(cudaError_t e) { return e == cudaSuccess ? RA_OK : RA_ERR_CUDA; }
+ra_status launch_result(cudaError_t e) { return e == cudaSuccess ? RA_OK : cuda_failed(e); }
 
 ra_status run_tc(const RingParams& p, cudaStream_t st) {
   // zigzag tiles by chunk: the contiguous view with X = 2P chunks of L = S/2 tokens
@@ -303,7 +312,7 @@ ra_status run_tc(const RingParams& p, cudaStream_t st) {
   if (!encode_rows(&tq, p.q, p.B, p.N, p.H, p.D, p.L, p.X, ml) ||
       !encode_rows(&tk, p.k, p.B, p.N, p.G, p.D, p.L, p.X, ml) ||
       !encode_rows(&tv, p.v, p.B, p.N, p.G, p.D, p.L, p.X, ml))
-    return RA_ERR_CUDA;
+    return cuda_failed(cudaErrorInvalidValue);
   return launch_result(launch_ring_tc(p, tq, tk, tv, st));
 }
 
@@ -528,15 +537,15 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   // the device's highest priority, so their blocks go ahead of the ring kernel's.
   int lo_prio = 0, hi_prio = 0;
   cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio);
-  if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_failed(e);
   cudaStream_t os = nullptr, own_is = nullptr;
   e = cudaStreamCreateWithPriority(&os, cudaStreamNonBlocking, hi_prio);
-  if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_failed(e);
   if (zq || zk || zv) {
     e = cudaStreamCreateWithPriority(&own_is, cudaStreamNonBlocking, hi_prio);
     if (e != cudaSuccess) {
       cudaStreamDestroy(os);
-      return RA_ERR_CUDA;
+      return cuda_failed(e);
     }
   }
   const cudaStream_t is = own_is ? own_is : static_cast<cudaStream_t>(copy_stream);
@@ -546,7 +555,7 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   if (ev == nullptr) {
     cudaStreamDestroy(os);
     if (own_is) cudaStreamDestroy(own_is);
-    return RA_ERR_CUDA;
+    return cuda_failed(cudaErrorMemoryAllocation);
   }
   int made = 0;
   for (; made < n_ev && e == cudaSuccess; ++made)
@@ -627,7 +636,7 @@ ra_status ring_attn_fwd_host(const ra_problem* pr, const void* q, const void* k,
   cudaStreamDestroy(os);                                      // likewise
   if (own_is) cudaStreamDestroy(own_is);
   if (st != RA_OK) return st;
-  return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+  return e == cudaSuccess ? RA_OK : cuda_failed(e);
 }
 
 int32_t ring_attn_host_mapped(const void* p, size_t bytes) {
@@ -860,7 +869,7 @@ ra_status ring_attn_bwd(const ra_problem* pr, const void* q, const void* k, cons
       !encode_rows(&tk, k, p.B, p.N, p.G, p.D, p.L, p.X, ml) ||
       !encode_rows(&tv, v, p.B, p.N, p.G, p.D, p.L, p.X, ml) ||
       !encode_ext(&text, ext, static_cast<int64_t>(p.tiles) * 2 * 128 + 128))
-    return RA_ERR_CUDA;
+    return cuda_failed(cudaErrorInvalidValue);
   if ((st = launch_result(launch_bwd_prep(p, s))) != RA_OK) return st;
   if ((st = launch_result(launch_bwd_dkdv(p, tq, tdo, tk, tv, text, s))) != RA_OK) return st;
   return launch_result(launch_bwd_dq(p, tq, tdo, tk, tv, s));
@@ -909,12 +918,12 @@ ra_status ring_attn_decode(const ra_problem* pr, int32_t n_q, int32_t q_pos0, co
   CUtensorMap tk, tv;
   if (!encode_rows(&tk, k, p.B, p.N, p.G, p.D, p.L, p.X, ml, 32) ||
       !encode_rows(&tv, v, p.B, p.N, p.G, p.D, p.L, p.X, ml, 32))
-    return RA_ERR_CUDA;
+    return cuda_failed(cudaErrorInvalidValue);
   p.o = o;
   p.lse = lse;
   const bool clustered = decode_clustered(p, n_q);
   cudaError_t e = launch_decode_partials(p, tk, tv, n_q, q_pos0, o_parts, lse_parts, clustered, cs);
-  if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_failed(e);
   if (clustered) return RA_OK;
   return launch_result(launch_merge(static_cast<int>(parts), pr->batch, n_q, pr->heads,
                                     pr->head_dim, o_parts, lse_parts, o, p.o_f32 != 0, lse,
@@ -928,8 +937,9 @@ ra_status ring_attn_last_error(int32_t* device_code) {
   if (st != RA_OK) return st;
   int code = 0;
   const int zero = 0;
-  if (cudaMemcpyFromSymbol(&code, g_status, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
-  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
+  cudaError_t e = cudaMemcpyFromSymbol(&code, g_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_failed(e);
+  if ((e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int))) != cudaSuccess) return cuda_failed(e);
   *device_code = code;
   return RA_OK;
 }
@@ -948,6 +958,12 @@ ra_status ring_attn_selftest_timeout(uint64_t limit_ns, void* stream) {
   return launch_result(launch_selftest_timeout(limit_ns, d->status, static_cast<cudaStream_t>(stream)));
 }
 
+int32_t ring_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* ring_attn_cuda_error_name(int32_t code) {
+  return cudaGetErrorName(static_cast<cudaError_t>(code));
+}
+
 const char* ra_status_str(ra_status s) {
   switch (s) {
     case RA_OK: return "RA_OK";
@@ -960,7 +976,7 @@ const char* ra_status_str(ra_status s) {
   return "RA_ERR_UNKNOWN";
 }
 
-int32_t ring_attn_version(void) { return 101; }
+int32_t ring_attn_version(void) { return 102; }
 
 int32_t ring_attn_debug_checks(void) { return kDebugChecks ? 1 : 0; }
 

@@ -35,7 +35,7 @@ def test_header_declarations_match_binding():
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name
-    assert lib.ring_attn_version() == 101
+    assert lib.ring_attn_version() == 102
 
 
 def test_debug_build_exports_the_same_symbols_and_reports_its_checks(lib):
@@ -61,6 +61,20 @@ def test_binding_constants_match_the_header():
 def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert lib.ra_status_str(code).decode() == name
+
+
+def test_cuda_error_behind_ra_err_cuda_is_reported(lib):
+    assert lib.ring_attn_cuda_error_name(0).decode() == "cudaSuccess"
+    assert lib.ring_attn_cuda_error_name(2).decode() == "cudaErrorMemoryAllocation"
+    if torch.cuda.is_available():
+        pytest.skip("needs a process without a usable GPU")
+    code = ctypes.c_int32(-1)
+    # without a GPU the call cannot find a device: RA_ERR_CUDA, and the CUDA error it got
+    assert lib.ring_attn_last_error(ctypes.byref(code)) == _lib.RA_ERR_CUDA
+    err = lib.ring_attn_last_cuda_error()
+    assert err != 0 and lib.ring_attn_cuda_error_name(err).decode().startswith("cudaError")
+    with pytest.raises(_lib.RingAttnError, match=r"RA_ERR_CUDA \(cudaError"):
+        _lib.check("ring_attn_last_error", lib.ring_attn_last_error(ctypes.byref(code)))
 
 
 def _pr(**kw):
@@ -153,8 +167,9 @@ def test_decode_workspace_and_argument_checks(lib):
     (2, 1040, 4, 8 * 2),        # zigzag: 8 chunks of 130 rows: 2 tiles each
     (0, 256, 1, 2),
 ])
-def test_bwd_workspace_bytes(lib, layout, N, P, tiles_per_bh):
-    pr = _pr(seqlen=N, P=P, layout=layout, heads=6, kv_heads=3, batch=2)
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_workspace_bytes(lib, layout, N, P, tiles_per_bh, d):
+    pr = _pr(seqlen=N, P=P, layout=layout, heads=6, kv_heads=3, batch=2, head_dim=d)
     # per query tile: 1 KiB of statistics and two 4 KiB extension tiles; one 4 KiB key-side tile
     assert lib.ring_attn_bwd_workspace_bytes(ctypes.byref(pr)) == \
         2 * 6 * tiles_per_bh * (1024 + 2 * 4096) + 4096
