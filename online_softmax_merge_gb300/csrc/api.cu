@@ -48,14 +48,16 @@ unsigned long long current_context_id() {
 }  // namespace ra
 
 namespace {
-
-// The CUDA error behind the calling thread's most recent RA_ERR_CUDA (0 before any);
-// cuda_failed records it and returns RA_ERR_CUDA.
+// The CUDA error behind the calling thread's most recent RA_ERR_CUDA (0 before any).
 thread_local int32_t g_last_cuda_error = 0;
-ra_status cuda_failed(cudaError_t e) {
+}  // namespace
+
+ra_status ra::cuda_failed(cudaError_t e) {
   g_last_cuda_error = static_cast<int32_t>(e);
   return RA_ERR_CUDA;
 }
+
+namespace {
 
 // Status word of the GPU: a kernel that gives up on a wait records its code here.
 __device__ int g_status = 0;

@@ -76,7 +76,8 @@ extern "C" ra_status ring_attn_decode_noalloc(const ra_problem* p, int32_t n_q, 
   if (need == 0) return RA_ERR_INVALID_ARG;                 // invalid problem or n_q
   if (need > ra::kScratchBytes) return RA_ERR_INVALID_ARG;  // partials do not fit the scratch
   void* scratch = nullptr;
-  if (ra::scratch_address(&scratch) != cudaSuccess) return RA_ERR_CUDA;
+  const cudaError_t e = ra::scratch_address(&scratch);
+  if (e != cudaSuccess) return ra::cuda_failed(e);
   // Every partial the decode writes is written before the merge reads it, so the
   // previous call's contents need no clearing.
   return ring_attn_decode(p, n_q, q_pos0, q, k, v, o, lse, scratch, ra::kScratchBytes, stream);

@@ -138,6 +138,10 @@ struct BwdParams {
   int* status;
 };
 
+// Records e as the calling thread's last CUDA error (ring_attn_last_cuda_error) and
+// returns RA_ERR_CUDA.
+ra_status cuda_failed(cudaError_t e);
+
 // Launchers (return a cudaError_t of the launch).
 cudaError_t launch_ring_tc(const RingParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t st);
