@@ -345,7 +345,7 @@ def workload_bytes(w, o_bytes: int = 2) -> int:
 
 def config_obj(w, args):
     preset = WORKLOADS[w.name]
-    changed = [f"{k}={getattr(w, k)}" for k in ("layout", "P", "seed")
+    changed = [f"{k}={getattr(w, k)}" for k in ("layout", "P", "seed", "head_dim")
                if getattr(w, k) != getattr(preset, k)]
     text = WORKLOAD_TEXT.get(w.name, "") + (f" (overridden: {', '.join(changed)})" if changed else "")
     return {"workload": f"{w.name}: {text}", "batch": w.batch,
@@ -446,7 +446,9 @@ def run_ours(args, w):
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     mean_launch_s = statistics.mean(launch_ms) * 1e-3
     achieved = flops_step / mean_launch_s / 1e12
-    traffic = load_traffic(f"ring_tc_kernel:{w.name}:{args.out_dtype}")
+    # the stored counters are of the preset workloads; an overridden one has none
+    traffic = (load_traffic(f"ring_tc_kernel:{w.name}:{args.out_dtype}")
+               if w == WORKLOADS[w.name] else None)
 
     # ---- the same forward writing O in the other element type (bf16 <-> fp32)
     other = None
@@ -671,6 +673,8 @@ def main():
     ap.add_argument("--layout", default=None, choices=[None, "contiguous", "striped", "zigzag"])
     ap.add_argument("--P", type=int, default=None, help="override the preset's shard count")
     ap.add_argument("--seed", type=int, default=None, help="override the preset's input seed")
+    ap.add_argument("--head-dim", type=int, default=None, choices=[64, 128],
+                    help="override the preset's head size (same tokens, heads and shards)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
@@ -695,6 +699,8 @@ def main():
         w = w.with_(P=args.P)
     if args.seed is not None:
         w = w.with_(seed=args.seed)
+    if args.head_dim is not None:
+        w = w.with_(head_dim=args.head_dim)
     if w.seqlen % w.P or (w.layout == "zigzag" and w.seqlen % (2 * w.P)):
         ap.error(f"--P {w.P} does not divide the {w.seqlen}-token sequence into "
                  f"{'2P chunks' if w.layout == 'zigzag' else 'shards'}")
