@@ -194,6 +194,17 @@ def test_bwd_c4_sampled():
     _sampled(w, rows, keys, groups=[3])
 
 
+def test_bwd_c4_shape_at_head_size_64_sampled():
+    """d = 64 on the c4 shape: both backward kernels keep a second score buffer there
+    (and dK/dV a third Q/dO stage)."""
+    w = WORKLOADS["c4"].with_(head_dim=64)
+    N = w.seqlen
+    rng = np.random.default_rng(16)
+    rows = sorted({0, 8191, 8192, N - 1} | set(rng.integers(0, N, 4).tolist()))
+    keys = [N - 1, N - 128, N - 300]
+    _sampled(w, rows, keys, groups=[0, 6])
+
+
 def test_bwd_c3_striped_sampled():
     w = WORKLOADS["c3"]
     N = w.seqlen

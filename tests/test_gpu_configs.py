@@ -172,6 +172,16 @@ def test_c4_sampled_with_stress_rows():
     _check_sampled("c4", w, w.layout, q, k, v, o32, o16, lse, sel)
 
 
+def test_c4_shape_at_head_size_64():
+    """The c4 workload at d = 64, where the kernel keeps a third score buffer in the
+    TMEM columns O leaves free: the same sample, stress rows included."""
+    w = WORKLOADS["c4"].with_(head_dim=64)
+    q, k, v = make_qkv(w, device=DEV)
+    o32, o16, lse = _fwd_both(w, q, k, v, w.layout)
+    sel, _ = _select(w, w.layout, o32, lse, seed=44, stress=stress_positions(w))
+    _check_sampled("c4-d64", w, w.layout, q, k, v, o32, o16, lse, sel)
+
+
 def test_c5_sampled():
     w = WORKLOADS["c5"]
     q, k, v = make_qkv(w, device=DEV)
