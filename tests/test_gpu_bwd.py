@@ -205,6 +205,20 @@ def test_bwd_c4_shape_at_head_size_64_sampled():
     _sampled(w, rows, keys, groups=[0, 6])
 
 
+def test_bwd_c4_zigzag_sampled():
+    """The c4 workload with the zigzag layout: every shard holds two chunks, so each
+    key tile meets the queries of both of its shard's segments."""
+    w = WORKLOADS["c4"].with_(layout="zigzag")
+    N = w.seqlen
+    rng = np.random.default_rng(17)
+    chunk = N // (2 * w.P)
+    rows = sorted({0, chunk - 1, chunk, N - chunk, N - 1} | set(rng.integers(0, N, 4).tolist()))
+    # late keys (the oracle's cost grows with the queries that see a key) in the last two
+    # chunks, which belong to different shards: chunk 2P-1 to shard 0, chunk 2P-2 to shard 1
+    keys = [N - 1, N - 100, N - chunk - 1]
+    _sampled(w, rows, keys, groups=[2])
+
+
 def test_bwd_c3_striped_sampled():
     w = WORKLOADS["c3"]
     N = w.seqlen

@@ -130,19 +130,20 @@ def test_c2_sampled_and_three_heads_in_full():
     _check_sampled("c2", w, w.layout, q, k, v, o32, o16, lse, sel)
 
 
-def test_c3_striped_and_contiguous_on_same_tensors():
+def test_c3_three_layouts_on_same_tensors():
     w = WORKLOADS["c3"]
     q, k, v = make_qkv(w, device=DEV)
     out = {}
-    for i, layout in enumerate(("striped", "contiguous")):
+    for i, layout in enumerate(("striped", "contiguous", "zigzag")):
         o32, o16, lse = _fwd_both(w, q, k, v, layout)
         sel, _ = _select(w, layout, o32, lse, seed=30 + i)
         _check_sampled("c3", w, layout, q, k, v, o32, o16, lse, sel)
         out[layout] = (o32, lse)
         del o16
-    # the layout is an index map: both orders of the same ring reach the same result
-    assert float((out["striped"][0] - out["contiguous"][0]).abs().max()) <= 2 * TOL_O
-    assert float((out["striped"][1] - out["contiguous"][1]).abs().max()) <= 2 * TOL_LSE
+    # the layout is an index map: every order of the same ring reaches the same result
+    for layout in ("contiguous", "zigzag"):
+        assert float((out["striped"][0] - out[layout][0]).abs().max()) <= 2 * TOL_O
+        assert float((out["striped"][1] - out[layout][1]).abs().max()) <= 2 * TOL_LSE
 
 
 def _argmax_keys(q, k, w, b, h, rows):
